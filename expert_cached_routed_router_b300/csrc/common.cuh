@@ -1,0 +1,101 @@
+// Shared definitions of the ft_moe CUDA library (device state layout, small helpers).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "ft_moe.h"
+
+namespace ftm {
+
+constexpr int kMaxE = 1024;        // experts per layer
+constexpr int kMaxK = 32;          // routed experts per token
+constexpr int kGemvMaxTokens = 16; // forward calls with T <= this use the GEMV kernels
+constexpr double kNearTie = 1e-6;  // top-k gap reported as a near-tie (exact fp32 difference)
+
+// Device counters and the status word.  One instance per handle, in device memory.
+struct DevCounters {
+  unsigned long long calls, hits, misses, fill_bytes, evictions, near_ties;
+  unsigned long long tick;       // global LRU clock
+  int status;                    // first device-side error (FT_ERR_*), 0 = none
+  int n_fill;                    // fills of the most recent forward call
+  int n_work;                    // work items of the most recent call
+  int occupied;                  // slots holding an entry
+  int call_status;               // 0, or FT_ERR_CAPACITY if the current call was refused
+  int pad[3];
+};
+
+// One group of rows of the expert FFN: the rows q0 .. q0+count-1 of the permuted
+// activations all use the weights of one complete entry W (W_gate | W_up | W_down).
+struct WorkItem {
+  const uint16_t *W;
+  int q0;
+  int count;
+  int expert;  // expert id, or -1 for the shared expert
+  int slot;    // cache slot (decode), expert id (prefill buffer) or -1 (shared)
+};
+
+// Arguments of the routing/control stage for one call.
+struct ControlArgs {
+  const int32_t *idx;   // [T][k]
+  const float *w;       // [T][k]
+  const uint8_t *tie;   // [T]
+  int T, k, E, P;       // P = T*k
+  int layer, L;
+  int32_t *counts;      // [E]
+  int32_t *offsets;     // [E+1]
+  int32_t *perm;        // [P]
+  int32_t *inv;         // [P]
+  int32_t *tok;         // [P + T] token of FFN row q
+  float *wq;            // [P + T] gate weight of FFN row q
+  WorkItem *work;       // [E + 1]
+  // cache (decode mode); null slot_table selects prefill mode
+  int32_t *slot_table;  // [L][E]
+  int32_t *owner;       // [n_slots]
+  unsigned long long *stamps;  // [n_slots]
+  int n_slots;
+  int32_t *fills;       // [max_fill][3]
+  const uint16_t *slots;       // slot storage
+  const uint16_t *buffer;      // prefill: E entries of this layer
+  const uint16_t *shared;      // shared entry of this layer or null
+  size_t entry_elems;
+  DevCounters *ctr;
+};
+
+__device__ __forceinline__ float bf16_to_f32(uint16_t b) {
+  return __uint_as_float(((uint32_t)b) << 16);
+}
+
+// Round to nearest even (no NaNs arise on this path).
+__device__ __forceinline__ uint16_t f32_to_bf16(float f) {
+  uint32_t u = __float_as_uint(f);
+  u += 0x7FFFu + ((u >> 16) & 1u);
+  return (uint16_t)(u >> 16);
+}
+
+__device__ __forceinline__ void set_status(DevCounters *c, int code) {
+  atomicCAS(&c->status, 0, code);
+}
+
+// Streaming 16-byte load that bypasses L1 allocation (weights are read once).
+__device__ __forceinline__ uint4 ld_stream(const void *p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+// Dot of 8 bf16 pairs packed in two uint4, accumulated sequentially in feature order.
+__device__ __forceinline__ float dot8_seq(uint4 a, uint4 b, float acc) {
+  const uint32_t av[4] = {a.x, a.y, a.z, a.w};
+  const uint32_t bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    acc = fmaf(__uint_as_float(av[i] << 16), __uint_as_float(bv[i] << 16), acc);
+    acc = fmaf(__uint_as_float(av[i] & 0xFFFF0000u), __uint_as_float(bv[i] & 0xFFFF0000u), acc);
+  }
+  return acc;
+}
+
+}  // namespace ftm

@@ -1,0 +1,209 @@
+/*
+ * ft_moe.h - routed Mixture-of-Experts layer forward with a device-resident LRU
+ * expert-slot cache, for one NVIDIA B300 (sm_103a).
+ *
+ * The system follows the FreeToken pages:
+ *   - "FreeToken benchmark", section "how FreeToken serves large MoE models": the full
+ *     routed-expert pool lives in host memory as the source of truth; the GPU holds an
+ *     elastic expert cache; prefill double-buffers whole layers (layer l+1 is copied while
+ *     layer l computes); decode uses a shared LRU expert cache; device-resident control
+ *     data keeps routing-dependent decisions compatible with captured CUDA execution
+ *     ("graph compatibility" blurb).
+ *   - "FreeToken RTX 4090", section "how the MoE memory hierarchy works": a cache entry is
+ *     one complete logical (layer, expert) pair, identified by one mapping on CPU and GPU;
+ *     the LRU is shared across layers and tokens and follows routing.
+ *   - "FreeToken vram": the GPU expert cache can be rebuilt at scheduler safe points
+ *     without restarting or reloading the host pool.
+ * The pages print no formulas.  The layer computed here (a reading, stated once):
+ *   logits l[t,e] = sum_i x[t,i] W_r[e,i] (+ bias[e]) in one fixed fp32 order;
+ *   top-k by (logit descending, expert id ascending);
+ *   gates = softmax over the k selected logits (= full softmax renormalised over top-k);
+ *   y_e(x) = W_down^T (silu(W_gate^T x) * (W_up^T x));
+ *   out[t] = sum_j w[t,j] y_{idx[t,j]}(x_t) (+ the shared expert with weight 1).
+ *
+ * Conventions for every call:
+ *   - Returns FT_OK (0) or a negative-free error code below; ft_last_error() gives a
+ *     thread-local message for the last failing call of this thread.
+ *   - "device" pointers are CUDA device memory of the current device; "host" pointers are
+ *     ordinary or pinned host memory as stated.
+ *   - bf16 tensors are row-major arrays of uint16 bit patterns.
+ *   - A handle is not thread-safe; calls on one handle must not overlap.
+ *   - Asynchronous calls (forward, set_router_bias) only enqueue work on the given stream;
+ *     device-side failures (capacity exceeded, a bad index caught by a kernel) are recorded
+ *     in a device status word read by ft_cache_stats() / ft_moe_status().
+ *   - No kernel traps, asserts or spins: kernels that meet an error set the status word and
+ *     return.
+ */
+#ifndef FT_MOE_H
+#define FT_MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *ft_stream_t; /* a cudaStream_t; NULL = legacy default stream */
+
+enum {
+  FT_OK = 0,
+  FT_ERR_INVALID = 1,  /* bad argument (shape, pointer, layer index, alignment)         */
+  FT_ERR_STATE = 2,    /* call not allowed now (no pool loaded, stream capture active)   */
+  FT_ERR_CUDA = 3,     /* a CUDA runtime call failed; message in ft_last_error()         */
+  FT_ERR_OOM = 4,      /* device or pinned allocation failed; state unchanged            */
+  FT_ERR_CAPACITY = 5, /* a call touched more distinct experts than there are slots      */
+  FT_ERR_TIMEOUT = 6   /* reserved for bounded device waits                              */
+};
+
+typedef struct ft_moe ft_moe;
+
+/* Options for ft_moe_create; pass NULL for the defaults given in brackets. */
+typedef struct {
+  int n_shared;     /* [0] 1 = one always-active shared expert per layer, outside the LRU */
+  int prewarm;      /* [1] fill the cache at ft_moe_load_pool with entries (l,e) in
+                           lexicographic order, slots 0..min(n_slots,L*E)-1, stamps 1..n  */
+  int max_tokens;   /* [4096] largest T accepted by forward / prefill (sizes scratch)     */
+  int debug_checks; /* [0] kernels re-check slot indices and record violations           */
+} ft_moe_opts;
+
+/* Cache counters, accumulated on the device since creation or the last reset. */
+typedef struct {
+  uint64_t calls;      /* forward calls that reached the cache                            */
+  uint64_t hits;       /* sum over calls of |touched experts already resident|            */
+  uint64_t misses;     /* sum over calls of |touched experts not resident| (= fills)      */
+  uint64_t fill_bytes; /* misses * entry bytes copied host -> slot                        */
+  uint64_t evictions;  /* resident entries replaced by a miss                             */
+  uint64_t near_ties;  /* tokens whose top-k decision had a logit gap <= 1e-6             */
+  uint64_t resizes;    /* successful ft_cache_resize calls                                */
+  uint64_t tick;       /* global LRU clock (last stamp handed out)                        */
+  int32_t n_slots;     /* current capacity in entries                                     */
+  int32_t occupied;    /* slots holding an entry                                          */
+  int32_t status;      /* first device-side error code since the last reset (0 = none)    */
+  int32_t reserved;
+} ft_cache_stats_t;
+
+/* Message for the last failing call on this thread ("" if none). */
+const char *ft_last_error(void);
+
+/*
+ * Create a layer stack: L layers, E routed experts per layer, top-k routing, hidden size d,
+ * expert FFN size d_ff, and a cache of n_slots complete (layer, expert) entries.
+ * Requires 1 <= k <= E <= 1024, k <= 32, d % 128 == 0, d_ff % 128 == 0, 1 <= n_slots,
+ * d <= 8192, d_ff <= 8192.
+ * One entry is 3*d*d_ff bf16: W_gate rows [d_ff][d], W_up rows [d_ff][d], W_down rows
+ * [d][d_ff] (each row one output feature, contiguous over input features).  The library
+ * allocates and owns all device state (router weights, slot storage, tables, scratch).
+ * *out receives the handle; on failure *out is NULL and nothing stays allocated.
+ */
+int ft_moe_create(int L, int E, int k, int d, int d_ff, int n_slots, const ft_moe_opts *opts,
+                  ft_moe **out);
+
+/* Free every device allocation; unregister the host pool if this library registered it.
+ * Synchronises the library's streams first.  NULL is ignored. */
+void ft_moe_destroy(ft_moe *h);
+
+/*
+ * Router weights of one layer: Wr = device bf16 [E][d] (copied), bias = device fp32 [E] or
+ * NULL (bias 0).  Synchronous.  The bias is added to the logits before top-k and before the
+ * gate softmax.
+ */
+int ft_moe_load_router(ft_moe *h, int layer, const void *Wr_bf16, const float *bias);
+
+/*
+ * Replace router biases on `stream` (device-to-device, so it may sit inside a captured
+ * graph): layer >= 0 sets that layer from device fp32 [E]; layer == -1 sets all layers from
+ * device fp32 [L][E].
+ */
+int ft_moe_set_router_bias(ft_moe *h, int layer, const float *bias, ft_stream_t stream);
+
+/*
+ * Attach the host expert pool: `host_pool` holds L*E entries in [L][E][entry] order,
+ * `bytes` == L*E*3*d*d_ff*2.  The caller owns the pool and keeps it alive and unchanged
+ * until ft_moe_destroy.  Pinned memory (cudaHostAlloc / cudaHostRegister) is used as is;
+ * pageable memory is registered here (mapped) and unregistered at destroy.  Kernels read
+ * missed entries straight from the mapped pool over the host link.  With prewarm, copies
+ * the first min(n_slots, L*E) entries into slots 0.. in (layer, expert) order.
+ * Synchronous.  Must be called once, before forward / prefill.
+ */
+int ft_moe_load_pool(ft_moe *h, void *host_pool, size_t bytes);
+
+/* Shared expert of one layer (opts.n_shared = 1): one entry, device or host bf16, copied. */
+int ft_moe_load_shared(ft_moe *h, int layer, const void *entry_bf16);
+
+/*
+ * Decode / general forward of one layer: x = device bf16 [T][d], out = device bf16 [T][d],
+ * 1 <= T <= max_tokens.  Runs router, top-k, permutation, the LRU update, fills of missed
+ * entries from the host pool, the SwiGLU experts through the slot table, and the weighted
+ * combine, all on `stream`, with no host synchronisation, so a sequence of calls can be
+ * captured into a CUDA graph (for a fixed T).  If the call touches more distinct experts
+ * than n_slots, the device status becomes FT_ERR_CAPACITY, the cache is unchanged and
+ * out is left unwritten.  x and out may not overlap.
+ */
+int ft_moe_forward(ft_moe *h, int layer, const void *x, int T, void *out, ft_stream_t stream);
+
+/*
+ * Decode step over consecutive layers from host buffers: copies x (host bf16 [T][d],
+ * pinned for full speed) to the device, runs ft_moe_forward for layers layer0 ..
+ * layer0+n_layers-1 on the same x, and copies the outputs to out (host bf16
+ * [n_layers][T][d]).  Enqueued on `stream`; synchronise before reading `out`.
+ */
+int ft_moe_decode_host(ft_moe *h, int layer0, int n_layers, const void *x_host, int T,
+                       void *out_host, ft_stream_t stream);
+
+/*
+ * Prefill with full-layer double buffering: for i = 0 .. n_layers-1, computes
+ * out[i] = MoE layer (layer0+i) applied to x (device bf16 [T][d]); out is device bf16
+ * [n_layers][T][d].  All E experts of layer l+1 are copied host -> device into the back
+ * buffer on an internal copy stream while layer l computes on `stream`.  Prefill reads
+ * the double buffer only: it neither reads nor updates the LRU cache.  Allocates the
+ * 2 x E-entry double buffer on first use.  Returns after enqueueing; `stream` waits for
+ * all of it.  Not capturable (FT_ERR_STATE during capture).
+ */
+int ft_moe_prefill_stream(ft_moe *h, int layer0, int n_layers, const void *x, int T, void *out,
+                          ft_stream_t stream);
+
+/* Timing of the most recent prefill (milliseconds, from CUDA events): per-layer copy and
+ * compute spans, summed, and the wall time from first copy to last compute. */
+int ft_moe_prefill_timing(ft_moe *h, float *copy_ms, float *compute_ms, float *wall_ms);
+
+/*
+ * Elastic resize at a safe point: synchronises the library's work, keeps the
+ * min(n_slots, occupied) most recently used entries (moved device-to-device into slots 0..
+ * in descending stamp order, stamps kept), frees the old slot storage.  Never reads the
+ * host pool.  FT_ERR_STATE while a stream capture is active; FT_ERR_OOM leaves the cache
+ * exactly as it was.
+ */
+int ft_cache_resize(ft_moe *h, int n_slots);
+
+/* Synchronise and copy the counters; ft_cache_stats_reset zeroes counters and status. */
+int ft_cache_stats(ft_moe *h, ft_cache_stats_t *out);
+int ft_cache_stats_reset(ft_moe *h);
+
+/* Synchronise and read the device status word (0 = no device-side error). */
+int ft_moe_status(ft_moe *h, int *status);
+
+/*
+ * Debug getters for the most recent forward / prefill layer (synchronise; host outputs):
+ *   routing:     idx int32 [T][k], w fp32 [T][k], tie uint8 [T]  (any may be NULL)
+ *   logits:      fp32 [T][E]
+ *   perm:        counts int32 [E], offsets int32 [E+1], perm int32 [T*k]
+ *   cache state: slot_table int32 [L][E] (-1 = absent), owner int32 [n_slots]
+ *                (layer*E+expert, -1 = free), stamps uint64 [n_slots], tick
+ *   fills:       n_fill, and fills int32 [n_fill][3] = (slot, layer, expert) in order;
+ *                `cap` = room in `fills` (entries)
+ */
+int ft_moe_get_routing(ft_moe *h, int32_t *idx, float *w, uint8_t *tie);
+int ft_moe_get_logits(ft_moe *h, float *logits);
+int ft_moe_get_perm(ft_moe *h, int32_t *counts, int32_t *offsets, int32_t *perm);
+int ft_moe_get_cache_state(ft_moe *h, int32_t *slot_table, int32_t *owner, uint64_t *stamps,
+                           uint64_t *tick);
+int ft_moe_get_fills(ft_moe *h, int32_t *n_fill, int32_t *fills, int cap);
+
+/* Sizes of a handle: [L, E, k, d, d_ff, n_slots, max_tokens, n_shared]. */
+int ft_moe_get_dims(ft_moe *h, int32_t dims[8]);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FT_MOE_H */

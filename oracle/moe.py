@@ -76,8 +76,8 @@ def topk(logits, k: int):
 
     Order: logit descending, expert id ascending among equal logits.  A token is reported
     as a near-tie when the k-th and (k+1)-th logits, or any two selected logits, are within
-    1e-6 of each other (fp32 differences): there a different summation order could pick a
-    different expert or rank.
+    1e-6 of each other (the exact difference of the fp32 logits): there a different summation
+    order could pick a different expert or rank.
     """
     logits = np.asarray(logits, dtype=np.float32)
     T, E = logits.shape
@@ -89,7 +89,7 @@ def topk(logits, k: int):
         sel = logits[t, order[:k]]
         if k < E and float(sel[-1]) - float(logits[t, order[k]]) <= NEAR_TIE:
             tie[t] = True
-        if k > 1 and np.min(np.diff(-sel)) <= NEAR_TIE:
+        if k > 1 and np.min(np.diff(-sel.astype(np.float64))) <= NEAR_TIE:
             tie[t] = True
     return idx, tie
 

@@ -1,0 +1,198 @@
+"""Parity of the CUDA path with the oracle on small seeded configurations (GPU)."""
+import numpy as np
+import pytest
+
+import ft_synth
+from oracle import lru as olru
+from oracle import moe as omoe
+
+from helpers import (Config, assert_cache_equal, assert_out_close, assert_routing_equal,
+                     make_stack, oracle_layer, out_bits_to_f64, to_dev_bf16)
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(st, l, x_bits):
+    import torch
+    x = to_dev_bf16(x_bits)
+    out = torch.empty_like(x)
+    st.forward(l, x, out)
+    torch.cuda.synchronize()
+    return out
+
+
+def test_tiny_layer_all_resident():
+    """d=256, d_ff=128, E=16 top-2, 64 tokens, 16 slots prewarmed: no misses, all bit-exact."""
+    cfg = Config(L=1, E=16, k=2, d=256, d_ff=128, n_slots=16)
+    st = make_stack(cfg, max_tokens=64)
+    x = ft_synth.activations(0, 0, 64, 256)
+    out = _run(st, 0, x)
+    ref = oracle_layer(cfg, 0, x)
+    np.testing.assert_array_equal(st.logits(64).view(np.uint32), ref["logits"].view(np.uint32))
+    assert_routing_equal(st, ref, 64)
+    assert_out_close(out_bits_to_f64(out), ref["out"])
+    s = st.stats()
+    assert s["misses"] == 0 and s["hits"] == len(set(ref["idx"].ravel())) and s["status"] == 0
+    assert len(st.fills()) == 0
+    st.close()
+
+
+@pytest.mark.parametrize("T", [1, 3, 4, 5, 16, 17, 40, 300])
+def test_layer_token_counts(T):
+    """GEMV path (T <= 16) and grouped-GEMM path (T > 16), ragged expert groups."""
+    cfg = Config(L=2, E=32, k=4, d=512, d_ff=384, n_slots=64, seed=1)
+    st = make_stack(cfg, max_tokens=512)
+    for l in range(2):
+        x = ft_synth.activations(1, 100 * T + l, T, cfg.d)
+        out = _run(st, l, x)
+        ref = oracle_layer(cfg, l, x)
+        np.testing.assert_array_equal(st.logits(T).view(np.uint32),
+                                      ref["logits"].view(np.uint32))
+        assert_routing_equal(st, ref, T)
+        assert_out_close(out_bits_to_f64(out), ref["out"])
+    assert st.status() == 0
+    st.close()
+
+
+def test_large_P_multi_cta_permutation():
+    """P = T*k > 1024 takes the multi-CTA grouping kernels."""
+    cfg = Config(L=1, E=64, k=6, d=256, d_ff=128, n_slots=64, seed=2)
+    T = 700
+    st = make_stack(cfg, max_tokens=T)
+    x = ft_synth.activations(2, 0, T, cfg.d)
+    out = _run(st, 0, x)
+    ref = oracle_layer(cfg, 0, x, tokens=np.arange(0, T, 7))
+    assert_routing_equal(st, ref, T)
+    assert_out_close(out_bits_to_f64(out)[ref["tokens"]], ref["out"])
+    st.close()
+
+
+@pytest.mark.parametrize("T", [1, 4, 6])
+def test_decode_trace_lru_bit_exact(T):
+    """A drifting-Zipf decode trace with evictions: routing, fills and the whole cache state
+    match the oracle simulator after every call; outputs within tolerance on every call."""
+    cfg = Config(L=3, E=16, k=2, d=256, d_ff=128, n_slots=12, seed=3)
+    st = make_stack(cfg, max_tokens=16)
+    sim = olru.SlotCacheSim(cfg.L, cfg.E, cfg.n_slots, cfg.entry_bytes, prewarm=True)
+    assert_cache_equal(st, sim)
+    gen = ft_synth.DriftingZipfBias(3, cfg.L, cfg.E, s=0.8, sigma_walk=0.3)
+    import torch
+    n_fills = 0
+    for step in range(25):
+        gen.advance()
+        x = ft_synth.activations(3, step, T, cfg.d)
+        for l in range(cfg.L):
+            b = gen.bias(l)
+            st.set_router_bias(l, torch.from_numpy(b).cuda())
+            out = _run(st, l, x)
+            ref = oracle_layer(cfg, l, x, bias=b)
+            assert_routing_equal(st, ref, T)
+            st_code, hits, fills = sim.access(l, ref["idx"].ravel())
+            assert st_code == olru.OK
+            got = st.fills()
+            np.testing.assert_array_equal(got, np.array([f[:3] for f in fills],
+                                                        dtype=np.int32).reshape(-1, 3))
+            n_fills += len(fills)
+            assert_cache_equal(st, sim)
+            assert_out_close(out_bits_to_f64(out), ref["out"])
+    s = st.stats()
+    assert s["misses"] == sim.misses == n_fills and s["hits"] == sim.hits
+    assert s["evictions"] == sim.evictions and s["status"] == 0
+    assert sim.evictions > 0
+    st.close()
+
+
+def test_capacity_error_leaves_cache_unchanged():
+    cfg = Config(L=1, E=16, k=4, d=256, d_ff=128, n_slots=3, seed=4)
+    st = make_stack(cfg, max_tokens=16)
+    before = st.cache_state()
+    x = ft_synth.activations(4, 0, 4, cfg.d)   # 4 tokens x top-4 touch > 3 experts
+    _run(st, 0, x)
+    after = st.cache_state()
+    for a, b in zip(before[:3], after[:3]):
+        np.testing.assert_array_equal(a, b)
+    assert before[3] == after[3]
+    assert st.status() == 5
+    st.stats_reset()
+    assert st.status() == 0
+    st.close()
+
+
+def test_resize_matches_simulator():
+    cfg = Config(L=2, E=16, k=2, d=256, d_ff=128, n_slots=8, seed=5)
+    st = make_stack(cfg, max_tokens=16)
+    sim = olru.SlotCacheSim(cfg.L, cfg.E, cfg.n_slots, cfg.entry_bytes, prewarm=True)
+    gen = ft_synth.DriftingZipfBias(5, cfg.L, cfg.E, s=0.5, sigma_walk=0.5)
+    import torch
+    step = 0
+
+    def run_steps(n):
+        nonlocal step
+        for _ in range(n):
+            gen.advance()
+            x = ft_synth.activations(5, step, 2, cfg.d)
+            step += 1
+            for l in range(cfg.L):
+                b = gen.bias(l)
+                st.set_router_bias(l, torch.from_numpy(b).cuda())
+                out = _run(st, l, x)
+                ref = oracle_layer(cfg, l, x, bias=b)
+                sim.access(l, ref["idx"].ravel())
+                assert_cache_equal(st, sim)
+                assert_out_close(out_bits_to_f64(out), ref["out"])
+
+    run_steps(6)
+    for n_new in (4, 12, 5):
+        st.resize(n_new)
+        sim.resize(n_new)
+        assert_cache_equal(st, sim)
+        run_steps(4)
+    assert st.stats()["resizes"] == 3
+    st.close()
+
+
+def test_shared_expert():
+    cfg = Config(L=2, E=16, k=3, d=256, d_ff=256, n_slots=20, n_shared=1, seed=6)
+    st = make_stack(cfg, max_tokens=64)
+    for T in (1, 7, 33):
+        x = ft_synth.activations(6, T, T, cfg.d)
+        out = _run(st, 1, x)
+        ref = oracle_layer(cfg, 1, x)
+        assert_routing_equal(st, ref, T)
+        assert_out_close(out_bits_to_f64(out), ref["out"])
+    st.close()
+
+
+def test_prefill_double_buffer_matches_oracle():
+    """Prefill reads the double buffer only: every layer on the same x, the cache untouched."""
+    import torch
+    cfg = Config(L=3, E=16, k=2, d=256, d_ff=128, n_slots=4, seed=7)
+    T = 600
+    st = make_stack(cfg, max_tokens=T)
+    before = st.cache_state()
+    x = ft_synth.activations(7, 0, T, cfg.d)
+    xd = to_dev_bf16(x)
+    out = torch.empty((3, T, cfg.d), dtype=torch.int16, device="cuda")
+    st.prefill(0, 3, xd, out)
+    torch.cuda.synchronize()
+    rows = np.arange(0, T, 5)
+    for l in range(3):
+        ref = oracle_layer(cfg, l, x, tokens=rows)
+        assert_out_close(out_bits_to_f64(out[l])[rows], ref["out"])
+    assert_routing_equal(st, oracle_layer(cfg, 2, x, tokens=[]), T)  # last layer's routing
+    after = st.cache_state()
+    for a, b in zip(before[:3], after[:3]):
+        np.testing.assert_array_equal(a, b)
+    c, k, w = st.prefill_timing()
+    assert c > 0 and k > 0 and w > 0
+    st.close()
+
+
+def test_forward_is_deterministic():
+    cfg = Config(L=1, E=32, k=4, d=512, d_ff=384, n_slots=32, seed=8)
+    st = make_stack(cfg, max_tokens=16)
+    x = ft_synth.activations(8, 0, 16, cfg.d)
+    a = _run(st, 0, x).cpu().numpy()
+    b = _run(st, 0, x).cpu().numpy()
+    np.testing.assert_array_equal(a, b)
+    st.close()
