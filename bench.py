@@ -1,0 +1,582 @@
+#!/usr/bin/env python3
+"""MoE-layer throughput on one B300: routed MoE layers with the device LRU expert-slot cache.
+
+Default workload ("decode24"): the decode trace of 24 layers, d=2048, d_ff=768, E=128
+routed experts, top-8, a global LRU pool of 768 slots (25% of the 3,072 layer-expert
+entries), router logits biased by a per-layer Zipf(1.1) popularity plus a slowly drifting
+random walk, misses filled from the pinned host pool.  A step is one decode step: the
+batch of b tokens through all 24 layers (router, top-k, grouping, LRU update, miss fills,
+SwiGLU experts, combine), captured once as a CUDA graph and replayed.  b = 1 is the headline;
+b = 4 and 16 are reported in ``config.per_batch``.  Inputs (activations, per-step biases)
+are resident in HBM before the timed region; every step streams >1.8 GB of expert weights,
+more than L2 (126 MB), so no flush is needed.
+
+Other workloads: ``--workload large8`` (8 layers, d=4096, d_ff=2048, E=256, top-6 + shared
+expert, 640 slots = 30 GiB), ``--workload prefill8`` (prefill streaming, 8 layers, T=4096 and
+16384).
+
+``--impl reference`` times the CPU oracle (the slow, plain reference implementation) on the
+same workload; each step is one layer call of the b=1 trace.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import signal
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOADS = {
+    "decode24": dict(L=24, E=128, k=8, d=2048, d_ff=768, n_slots=768, zipf=1.1, shared=0,
+                     batches=(1, 4, 16), headline_b=1),
+    "large8": dict(L=8, E=256, k=6, d=4096, d_ff=2048, n_slots=640, zipf=1.0, shared=1,
+                   batches=(1, 4, 16), headline_b=1),
+    "prefill8": dict(L=8, E=256, k=6, d=4096, d_ff=2048, n_slots=16, shared=0,
+                     tokens=(4096, 16384)),
+}
+SEED = 0
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return dict(hbm_gbs=d["hbm_gbs"], bf16=d["bf16_tflops"],
+                    bf16_sustained=d.get("bf16_tflops_sustained"), source="measured")
+    return dict(hbm_gbs=6400.0, bf16=1800.0, bf16_sustained=1400.0, source="fallback")
+
+
+# ----------------------------------------------------------------------------------------
+# clocks during the timed region
+# ----------------------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index=0):
+        self.dev = device_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.dev}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.send_signal(signal.SIGTERM)
+            self.proc.wait()
+
+    def summary(self):
+        rows = []
+        if self.path and os.path.exists(self.path):
+            for line in open(self.path):
+                f = [x.strip() for x in line.split(",")]
+                if len(f) >= 9:
+                    rows.append(f)
+            os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4)
+                          if r[5 + i].lower() == "active"})
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": float(rows[0][2]) if rows[0][2].replace(".", "").isdigit() else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ----------------------------------------------------------------------------------------
+# distributed plumbing (N > 1: independent replicas, no data-path collective)
+# ----------------------------------------------------------------------------------------
+def dist_setup(args):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v, world):
+    if world <= 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------------------
+# workload construction
+# ----------------------------------------------------------------------------------------
+def build_pool(wl, seed):
+    import torch
+    import ft_synth.gpu as sg
+    sg.build()
+    n = wl["L"] * wl["E"] * 3 * wl["d"] * wl["d_ff"]
+    pool = torch.empty(n, dtype=torch.int16, pin_memory=True)
+    sg.fill_pool(pool.data_ptr(), seed, wl["L"], wl["E"], wl["d"], wl["d_ff"])
+    return pool
+
+
+def make_stack(wl, pool, seed, max_tokens, n_slots=None):
+    import torch
+    import ft_synth
+    from expert_cached_routed_router_b300 import MoELayerStack
+    st = MoELayerStack(wl["L"], wl["E"], wl["k"], wl["d"], wl["d_ff"],
+                       n_slots or wl["n_slots"], n_shared=wl["shared"], max_tokens=max_tokens)
+    for l in range(wl["L"]):
+        wr = ft_synth.router_weight(seed, l, wl["E"], wl["d"])
+        st.load_router(l, torch.from_numpy(wr.view(np.int16)).cuda())
+        if wl["shared"]:
+            sh = ft_synth.shared_entry(seed, l, wl["d"], wl["d_ff"])
+            st.load_shared(l, torch.from_numpy(sh.view(np.int16)).cuda())
+    st.load_pool(pool, pool.numel() * 2)
+    torch.cuda.synchronize()
+    return st
+
+
+def decode_trace(wl, b, n_steps, seed):
+    """Device-resident (x [n][b][d] bf16, bias [n][L][E] fp32) for steps 1..n."""
+    import torch
+    import ft_synth
+    import ft_synth.gpu as sg
+    gen = ft_synth.DriftingZipfBias(seed, wl["L"], wl["E"], s=wl["zipf"])
+    bias = np.empty((n_steps, wl["L"], wl["E"]), np.float32)
+    for t in range(n_steps):
+        gen.advance()
+        for l in range(wl["L"]):
+            bias[t, l] = gen.bias(l)
+    x = torch.empty((n_steps, b, wl["d"]), dtype=torch.int16, device="cuda")
+    sg.activations_device(x.data_ptr(), seed, [1_000_000 * b + t for t in range(n_steps)], b,
+                          wl["d"], torch.cuda.current_stream().cuda_stream)
+    return x, torch.from_numpy(bias).cuda(), bias
+
+
+# ----------------------------------------------------------------------------------------
+# decode benchmark
+# ----------------------------------------------------------------------------------------
+def bench_decode_batch(wl, pool, b, W, K, seed, world):
+    import torch
+    L, d = wl["L"], wl["d"]
+    x_all, bias_all, _ = decode_trace(wl, b, W + K, seed)
+    st = make_stack(wl, pool, seed, max_tokens=max(16, b))
+    xs = torch.empty((b, d), dtype=torch.int16, device="cuda")
+    bs = torch.empty((L, wl["E"]), dtype=torch.float32, device="cuda")
+    out = torch.empty((L, b, d), dtype=torch.int16, device="cuda")
+
+    def step_body():
+        st.set_router_bias(-1, bs)
+        for l in range(L):
+            st.forward(l, xs, out[l])
+
+    # capture one decode step
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        xs.copy_(x_all[0])
+        bs.copy_(bias_all[0])
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    st.stats_reset()
+    # capture performs no work; the state only changes on replay
+    with torch.cuda.graph(g):
+        step_body()
+    torch.cuda.synchronize()
+
+    def run(t):
+        xs.copy_(x_all[t])
+        bs.copy_(bias_all[t])
+        g.replay()
+
+    for t in range(W):
+        run(t)
+    torch.cuda.synchronize()
+    st0 = st.stats()
+    barrier(world)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        e0.record()
+        for t in range(W, W + K):
+            run(t)
+        e1.record()
+        torch.cuda.synchronize()
+    barrier(world)
+    ms = e0.elapsed_time(e1)
+    st1 = st.stats()
+    assert st1["status"] == 0, f"device status {st1['status']}"
+    dh = st1["hits"] - st0["hits"]
+    dm = st1["misses"] - st0["misses"]
+    res = dict(b=b, ms=ms, ms_per_step=ms / K, tok_s=b * K / (ms / 1e3), hits=dh, misses=dm,
+               hit_rate=dh / max(1, dh + dm), fill_bytes=st1["fill_bytes"] - st0["fill_bytes"],
+               clocks=clk.summary())
+    del g
+    st.close()
+    return res, x_all, bias_all
+
+
+def profile_decode_batch(wl, pool, b, x_all, bias_all, W, K, seed):
+    """Per-kernel device time over the same trace steps (events around each launch)."""
+    import torch
+    from expert_cached_routed_router_b300 import PROF_CLASSES
+    L = wl["L"]
+    st = make_stack(wl, pool, seed, max_tokens=max(16, b))
+    out = torch.empty((L, b, wl["d"]), dtype=torch.int16, device="cuda")
+    for t in range(W):
+        st.set_router_bias(-1, bias_all[t])
+        for l in range(L):
+            st.forward(l, x_all[t], out[l])
+    torch.cuda.synchronize()
+    s0 = st.stats()
+    st.profile(True)
+    st.profile_read()
+    for t in range(W, W + K):
+        st.set_router_bias(-1, bias_all[t])
+        for l in range(L):
+            st.forward(l, x_all[t], out[l])
+    prof = st.profile_read()
+    st.profile(False)
+    s1 = st.stats()
+    touched = (s1["hits"] - s0["hits"]) + (s1["misses"] - s0["misses"])
+    fill_bytes = s1["fill_bytes"] - s0["fill_bytes"]
+    st.close()
+    return prof, touched, fill_bytes, K * L
+
+
+def bench_decode_e2e(wl, pool, b, x_all, bias_all, W, K, seed, world):
+    """Same trace through ft_moe_decode_host: x from pinned host memory each step, outputs
+    read back to pinned host memory each step, copies inside the timed region."""
+    import torch
+    L, d = wl["L"], wl["d"]
+    st = make_stack(wl, pool, seed, max_tokens=max(16, b))
+    xh = x_all[:W + K].cpu().pin_memory()
+    oh = torch.empty((L, b, d), dtype=torch.int16, pin_memory=True)
+    for t in range(W):
+        st.set_router_bias(-1, bias_all[t])
+        st.decode_host(0, L, xh[t], oh)
+    torch.cuda.synchronize()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for t in range(W, W + K):
+        st.set_router_bias(-1, bias_all[t])
+        st.decode_host(0, L, xh[t], oh)
+    e1.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    ms = e0.elapsed_time(e1)
+    st.close()
+    return dict(ms=ms, tok_s=b * K / (ms / 1e3), h2d=b * d * 2, d2h=L * b * d * 2)
+
+
+def cpu_oracle_decode(wl, pool, b, bias_np, seed, budget_s=15.0, max_calls=None):
+    """The oracle as it stands on layer calls of the trace, in order, until ``budget_s``."""
+    import ft_synth
+    from oracle import lru as olru
+    from oracle import moe as omoe
+    L, E, k, d, d_ff = wl["L"], wl["E"], wl["k"], wl["d"], wl["d_ff"]
+    ent = 3 * d * d_ff
+    pv = pool.numpy().view(np.uint16)
+    sim = olru.SlotCacheSim(L, E, wl["n_slots"], 2 * ent, prewarm=True)
+    routers = {}
+    calls = 0
+    t0 = time.perf_counter()
+    step = 0
+    while True:
+        x = ft_synth.activations(seed, 1_000_000 * b + step, b, d)
+        for l in range(L):
+            if l not in routers:
+                routers[l] = ft_synth.router_weight(seed, l, E, d)
+            r = omoe.moe_layer(x, routers[l], k,
+                               lambda e, l=l: pv[(l * E + e) * ent:(l * E + e + 1) * ent],
+                               d, d_ff, bias=bias_np[step, l],
+                               shared_entry=(ft_synth.shared_entry(seed, l, d, d_ff)
+                                             if wl["shared"] else None))
+            sim.access(l, r["idx"].ravel())
+            calls += 1
+            el = time.perf_counter() - t0
+            if (max_calls and calls >= max_calls) or (not max_calls and el >= budget_s):
+                return calls, el
+        step += 1
+
+
+def roofline_decode(wl, prof, touched, n_calls, pk):
+    """Achieved HBM GB/s of the gate/up GEMV (the largest HBM consumer of the step)."""
+    d, d_ff = wl["d"], wl["d_ff"]
+    gate_bytes = touched * 2 * d_ff * d * 2
+    down_bytes = touched * d * d_ff * 2
+    g_ms, g_n = prof["gateup"]
+    dn_ms, dn_n = prof["down"]
+    out = {}
+    for name, byt, ms, n in (("gateup", gate_bytes, g_ms, g_n), ("down", down_bytes, dn_ms, dn_n)):
+        gbs = byt / (ms / 1e3) / 1e9 if ms > 0 else 0.0
+        out[name] = dict(achieved=gbs, ms=ms, launches=n, bytes=byt)
+    return out
+
+
+def run_decode(args, wl, rank, world):
+    import torch
+    pk = peaks()
+    seed = SEED + rank
+    pool = build_pool(wl, seed)
+    per_batch = {}
+    head = None
+    for b in wl["batches"]:
+        res, x_all, bias_all = bench_decode_batch(wl, pool, b, args.warmup, args.steps, seed,
+                                                  world)
+        res["ms"] = max_over_ranks(res["ms"], world)
+        res["tok_s_all"] = world * b * args.steps / (res["ms"] / 1e3)
+        prof_k = min(args.steps, args.profile_steps)
+        prof, touched, fill_bytes, n_calls = profile_decode_batch(
+            wl, pool, b, x_all, bias_all, args.warmup, prof_k, seed)
+        rl = roofline_decode(wl, prof, touched, n_calls, pk)
+        fill_ms = prof["fill"][0]
+        res["kernels_ms_per_step"] = {c: v[0] / prof_k for c, v in prof.items()}
+        res["gateup_gbs"] = rl["gateup"]["achieved"]
+        res["down_gbs"] = rl["down"]["achieved"]
+        res["fill_gbs"] = fill_bytes / (fill_ms / 1e3) / 1e9 if fill_ms > 0 else None
+        e2e = bench_decode_e2e(wl, pool, b, x_all, bias_all, args.warmup, args.steps, seed, world)
+        e2e["ms"] = max_over_ranks(e2e["ms"], world)
+        res["e2e_tok_s_all"] = world * b * args.steps / (e2e["ms"] / 1e3)
+        res["e2e"] = e2e
+        per_batch[b] = res
+        if b == wl["headline_b"]:
+            head = (res, rl, prof, prof_k, bias_all)
+        del x_all, bias_all
+        torch.cuda.empty_cache()
+    res, rl, prof, prof_k, bias_all = head
+    b = wl["headline_b"]
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        calls, el = cpu_oracle_decode(wl, pool, b, bias_all.cpu().numpy(), seed,
+                                      budget_s=args.cpu_budget)
+        cpu = {"value": b * calls / wl["L"] / el, "unit": "tokens/s", "cores": 1,
+               "kind": "oracle",
+               "sample": f"first {calls} layer calls of the b={b} trace "
+                         f"({calls / wl['L']:.2f} decode steps), {el:.1f} s, numpy fp32 router "
+                         f"+ fp64 experts, single thread"}
+    g = rl["gateup"]
+    roof = {"bound": "hbm", "kernel": "k_gateup_gemv (gate/up + SwiGLU, decode)",
+            "achieved": round(g["achieved"], 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+            "frac": round(g["achieved"] / pk["hbm_gbs"], 4), "traffic": None,
+            "peak_source": pk["source"],
+            "algorithmic_bytes": "touched experts x 2*d_ff*d*2 B per call"}
+    line = {
+        "metric": "MoE-layer tokens/s (decode trace, b=1)",
+        "value": round(res["tok_s_all"], 2), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(res["ms"] / args.steps, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": args.workload, "layers": wl["L"], "d": wl["d"],
+                   "d_ff": wl["d_ff"], "experts": wl["E"], "top_k": wl["k"],
+                   "n_slots": wl["n_slots"], "batch": b, "graph": True,
+                   "l2": "inputs larger than L2 (every step streams >1.8 GB of experts)",
+                   "parallelism": f"replicas x{world}",
+                   "per_batch": {str(bb): {k: (round(v, 4) if isinstance(v, float) else v)
+                                           for k, v in r.items()
+                                           if k not in ("clocks", "e2e")}
+                                 for bb, r in per_batch.items()}},
+        "roofline": roof,
+        "roofline_down": {"achieved": round(rl["down"]["achieved"], 1), "unit": "GB/s",
+                          "frac": round(rl["down"]["achieved"] / pk["hbm_gbs"], 4)},
+        "cpu_baseline": cpu,
+        "e2e": {"value": round(res["e2e_tok_s_all"], 2), "unit": "tokens/s",
+                "h2d_bytes_per_step": res["e2e"]["h2d"], "d2h_bytes_per_step": res["e2e"]["d2h"]},
+        "gpu_launches": int(sum(v[1] for v in prof.values()) / prof_k * args.steps),
+        "clocks": res["clocks"],
+    }
+    return line
+
+
+# ----------------------------------------------------------------------------------------
+# prefill benchmark
+# ----------------------------------------------------------------------------------------
+def run_prefill(args, wl, rank, world):
+    """Prefill streaming: every layer's full expert set is copied host -> device into the back
+    buffer while the previous layer computes.  A step is one prefill over all L layers."""
+    import torch
+    import ft_synth.gpu as sg
+    pk = peaks()
+    seed = SEED + rank
+    pool = build_pool(wl, seed)
+    L, d, d_ff, k = wl["L"], wl["d"], wl["d_ff"], wl["k"]
+    K = max(1, min(args.steps, args.prefill_steps))
+    W = 1
+    per_T = {}
+    for T in wl["tokens"]:
+        st = make_stack(wl, pool, seed, max_tokens=T)
+        x = torch.empty((T, d), dtype=torch.int16, device="cuda")
+        sg.activations_device(x.data_ptr(), seed, [7_000_000 + T], T, d,
+                              torch.cuda.current_stream().cuda_stream)
+        out = torch.empty((L, T, d), dtype=torch.int16, device="cuda")
+        for _ in range(W):
+            st.prefill(0, L, x, out)
+        torch.cuda.synchronize()
+        barrier(world)
+        copy_ms = comp_ms = wall_ms = 0.0
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with ClockSampler(torch.cuda.current_device()) as clk:
+            e0.record()
+            for _ in range(K):
+                st.prefill(0, L, x, out)
+                c, kk, w = st.prefill_timing()
+                copy_ms += c
+                comp_ms += kk
+                wall_ms += w
+            e1.record()
+            torch.cuda.synchronize()
+        ms = max_over_ranks(e0.elapsed_time(e1), world)
+        # GEMM time alone (one profiled prefill)
+        st.profile(True)
+        st.profile_read()
+        st.prefill(0, L, x, out)
+        prof = st.profile_read()
+        st.profile(False)
+        flops = 2.0 * 3 * d * d_ff * T * k * L
+        gemm_ms = prof["gateup"][0] + prof["down"][0]
+        tflops = flops / (gemm_ms / 1e3) / 1e12 if gemm_ms > 0 else 0.0
+        overlap = (copy_ms + comp_ms - wall_ms) / max(1e-9, min(copy_ms, comp_ms))
+        per_T[T] = dict(ms_per_prefill=ms / K, tok_s=world * T * K / (ms / 1e3),
+                        gemm_ms_per_layer=gemm_ms / L, gemm_tflops=tflops,
+                        tc_frac=tflops / pk["bf16"], copy_ms=copy_ms / K,
+                        compute_ms=comp_ms / K, wall_ms=wall_ms / K, overlap=overlap,
+                        h2d_gbs=L * wl["E"] * 3 * d * d_ff * 2 / (copy_ms / K / 1e3) / 1e9,
+                        kernels_ms={c: v[0] for c, v in prof.items()}, clocks=clk.summary())
+        st.close()
+        del x, out
+        torch.cuda.empty_cache()
+    Th = wl["tokens"][-1]
+    r = per_T[Th]
+    return {
+        "metric": f"MoE-layer prefill tokens/s (T={Th}, 8 layers streamed)",
+        "value": round(r["tok_s"], 1), "unit": "tokens/s", "n_gpus": world, "steps": K,
+        "warmup": W, "ms_per_step": round(r["ms_per_prefill"], 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": args.workload, "layers": L, "d": d, "d_ff": d_ff,
+                   "experts": wl["E"], "top_k": k, "tokens": list(wl["tokens"]),
+                   "per_T": {str(t): {kk: (round(v, 4) if isinstance(v, float) else v)
+                                      for kk, v in rr.items()} for t, rr in per_T.items()}},
+        "roofline": {"bound": "tensor", "kernel": "grouped GEMM gate/up + down",
+                     "achieved": round(r["gemm_tflops"], 1), "peak": pk["bf16"],
+                     "unit": "TFLOP/s", "frac": round(r["tc_frac"], 4), "traffic": None,
+                     "peak_source": pk["source"]},
+        "e2e": None, "clocks": r["clocks"],
+    }
+
+
+# ----------------------------------------------------------------------------------------
+# reference arm: the CPU oracle on the same workload
+# ----------------------------------------------------------------------------------------
+def run_reference(args, wl, rank, world):
+    import torch
+    if rank != 0:
+        return None
+    b = wl["headline_b"]
+    seed = SEED
+    n = wl["L"] * wl["E"] * 3 * wl["d"] * wl["d_ff"]
+    import ft_synth.gpu as sg
+    sg.build()
+    pool = torch.empty(n, dtype=torch.int16, pin_memory=True)
+    sg.fill_pool(pool.data_ptr(), seed, wl["L"], wl["E"], wl["d"], wl["d_ff"])
+    n_steps = (args.warmup + args.steps) // wl["L"] + 2
+    import ft_synth
+    gen = ft_synth.DriftingZipfBias(seed, wl["L"], wl["E"], s=wl["zipf"])
+    bias = np.empty((n_steps, wl["L"], wl["E"]), np.float32)
+    for t in range(n_steps):
+        gen.advance()
+        for l in range(wl["L"]):
+            bias[t, l] = gen.bias(l)
+    cpu_oracle_decode(wl, pool, b, bias, seed, max_calls=max(1, args.warmup))
+    t0 = time.perf_counter()
+    calls, el = cpu_oracle_decode(wl, pool, b, bias, seed, max_calls=args.steps)
+    tok_s = b * calls / wl["L"] / el
+    return {
+        "impl": "reference", "metric": "MoE-layer tokens/s (decode trace, b=1)",
+        "value": round(tok_s, 4), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(el * 1e3 / args.steps, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": args.workload, "layers": wl["L"], "d": wl["d"],
+                   "d_ff": wl["d_ff"], "experts": wl["E"], "top_k": wl["k"],
+                   "n_slots": wl["n_slots"], "batch": b,
+                   "step": "one layer call of the b=1 decode trace (oracle)"},
+        "cpu_baseline": {"value": round(tok_s, 4), "unit": "tokens/s", "cores": 1,
+                         "kind": "oracle",
+                         "sample": f"{calls} layer calls of the b={b} trace, single thread"},
+        "e2e": {"value": round(tok_s, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__,
+                                 formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="decode24")
+    ap.add_argument("--profile-steps", type=int, default=100)
+    ap.add_argument("--prefill-steps", type=int, default=2)
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    wl = dict(WORKLOADS[args.workload])
+    import torch
+    if args.impl == "reference":
+        rank = int(os.environ.get("RANK", "0"))
+        line = run_reference(args, wl, rank, int(os.environ.get("WORLD_SIZE", "1")))
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+    rank, world, _ = dist_setup(args)
+    import expert_cached_routed_router_b300 as ftm
+    ftm.load_library()
+    if args.workload == "prefill8":
+        line = run_prefill(args, wl, rank, world)
+    else:
+        line = run_decode(args, wl, rank, world)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -27,8 +27,10 @@ EXPORTS = [
     "ft_moe_decode_host", "ft_moe_prefill_stream", "ft_moe_prefill_timing", "ft_cache_resize",
     "ft_cache_stats", "ft_cache_stats_reset", "ft_moe_status", "ft_moe_get_routing",
     "ft_moe_get_logits", "ft_moe_get_perm", "ft_moe_get_cache_state", "ft_moe_get_fills",
-    "ft_moe_get_dims",
+    "ft_moe_get_dims", "ft_moe_profile", "ft_moe_profile_read",
 ]
+
+PROF_CLASSES = ["router", "topk", "control", "fill", "gateup", "down", "other"]
 
 
 class FtError(RuntimeError):
@@ -92,6 +94,8 @@ def load_library(path: str = LIB_PATH):
         "ft_moe_get_cache_state": (I, [P, P, P, P, ctypes.POINTER(ctypes.c_uint64)]),
         "ft_moe_get_fills": (I, [P, ctypes.POINTER(ctypes.c_int32), P, I]),
         "ft_moe_get_dims": (I, [P, P]),
+        "ft_moe_profile": (I, [P, I]),
+        "ft_moe_profile_read": (I, [P, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -254,6 +258,19 @@ def ft_moe_get_fills(h, cap=1024):
     return fills[:min(n.value, cap)].copy()
 
 
+def ft_moe_profile(h, enable):
+    _check(load_library().ft_moe_profile(h, 1 if enable else 0))
+
+
+def ft_moe_profile_read(h) -> dict:
+    """{class: (total ms, launches)} since the last read."""
+    import numpy as np
+    ms = np.zeros(len(PROF_CLASSES), np.float64)
+    n = np.zeros(len(PROF_CLASSES), np.int64)
+    _check(load_library().ft_moe_profile_read(h, ms.ctypes.data, n.ctypes.data))
+    return {c: (float(ms[i]), int(n[i])) for i, c in enumerate(PROF_CLASSES)}
+
+
 class MoELayerStack:
     """One ft_moe handle: L routed-MoE layers sharing one LRU expert-slot cache."""
 
@@ -326,3 +343,9 @@ class MoELayerStack:
 
     def fills(self):
         return ft_moe_get_fills(self.h, cap=max(self.E, 1))
+
+    def profile(self, enable):
+        ft_moe_profile(self.h, enable)
+
+    def profile_read(self):
+        return ft_moe_profile_read(self.h)

@@ -307,12 +307,17 @@ __global__ void __launch_bounds__(256) k_gemm_simt(const WorkItem *__restrict__ 
   }
 }
 
-void launch_gemm_ffn(const WorkItem *work, const DevCounters *ctr, int max_work, int max_rows,
-                     const uint16_t *xp, uint16_t *h, const int32_t *tok, const float *wq,
-                     float *acc, int d, int d_ff, cudaStream_t s) {
+void launch_gemm_gateup(const WorkItem *work, const DevCounters *ctr, int max_work, int max_rows,
+                        const uint16_t *xp, uint16_t *h, int d, int d_ff, cudaStream_t s) {
   const unsigned my = (unsigned)((max_rows + kTM - 1) / kTM);
   dim3 g1((d_ff + kTN - 1) / kTN, my, max_work);
-  k_gemm_simt<true><<<g1, 256, 0, s>>>(work, ctr, xp, h, tok, wq, acc, d, d_ff);
+  k_gemm_simt<true><<<g1, 256, 0, s>>>(work, ctr, xp, h, nullptr, nullptr, nullptr, d, d_ff);
+}
+
+void launch_gemm_down(const WorkItem *work, const DevCounters *ctr, int max_work, int max_rows,
+                      const uint16_t *h, const int32_t *tok, const float *wq, float *acc, int d,
+                      int d_ff, cudaStream_t s) {
+  const unsigned my = (unsigned)((max_rows + kTM - 1) / kTM);
   dim3 g2((d + kTN - 1) / kTN, my, max_work);
   k_gemm_simt<false><<<g2, 256, 0, s>>>(work, ctr, h, nullptr, tok, wq, acc, d, d_ff);
 }

@@ -96,6 +96,13 @@ struct ft_moe {
   // most recent call, for the debug getters
   int last_T = 0;
   cudaStream_t last_stream = nullptr;
+
+  // kernel timing (ft_moe_profile)
+  bool prof_on = false;
+  std::vector<cudaEvent_t> prof_events;       // pool; pairs (begin, end)
+  std::vector<int> prof_class;                // class of pair i
+  double prof_ms[FT_PROF_N] = {};
+  int64_t prof_n[FT_PROF_N] = {};
 };
 
 namespace {
@@ -117,6 +124,47 @@ int alloc_n(ft_moe *h, T **p, size_t n) {
   return dev_alloc(h, reinterpret_cast<void **>(p), n * sizeof(T));
 }
 
+// Sum the recorded event pairs into prof_ms / prof_n and clear the record.
+void prof_flush(ft_moe *h) {
+  if (h->prof_class.empty()) return;
+  cudaEventSynchronize(h->prof_events[2 * h->prof_class.size() - 1]);
+  for (size_t i = 0; i < h->prof_class.size(); ++i) {
+    float ms = 0.f;
+    if (cudaEventElapsedTime(&ms, h->prof_events[2 * i], h->prof_events[2 * i + 1]) == cudaSuccess) {
+      h->prof_ms[h->prof_class[i]] += ms;
+      h->prof_n[h->prof_class[i]] += 1;
+    }
+  }
+  cudaGetLastError();
+  h->prof_class.clear();
+}
+
+// Brackets one kernel launch with timing events while profiling is on.
+struct ProfScope {
+  ft_moe *h;
+  cudaStream_t s;
+  int idx = -1;
+  ProfScope(ft_moe *h_, int cls, cudaStream_t s_) : h(h_), s(s_) {
+    if (!h->prof_on) return;
+    if (2 * (h->prof_class.size() + 1) > h->prof_events.size()) {
+      if (h->prof_events.size() < 16384) {
+        for (int i = 0; i < 512; ++i) {
+          cudaEvent_t e;
+          if (cudaEventCreate(&e) != cudaSuccess) break;
+          h->prof_events.push_back(e);
+        }
+      }
+      if (2 * (h->prof_class.size() + 1) > h->prof_events.size()) prof_flush(h);
+    }
+    idx = (int)h->prof_class.size();
+    h->prof_class.push_back(cls);
+    cudaEventRecord(h->prof_events[2 * idx], s);
+  }
+  ~ProfScope() {
+    if (idx >= 0) cudaEventRecord(h->prof_events[2 * idx + 1], s);
+  }
+};
+
 void free_all(ft_moe *h) {
   for (void *p : h->allocs) cudaFree(p);
   h->allocs.clear();
@@ -131,6 +179,7 @@ void free_all(ft_moe *h) {
     for (cudaEvent_t e : *v) cudaEventDestroy(e);
   if (h->copy_stream) cudaStreamDestroy(h->copy_stream);
   if (h->pool_registered) cudaHostUnregister(const_cast<uint16_t *>(h->pool_host));
+  for (cudaEvent_t e : h->prof_events) cudaEventDestroy(e);
 }
 
 bool capturing(cudaStream_t s) {
@@ -176,11 +225,18 @@ ControlArgs control_args(ft_moe *h, int layer, int T, bool decode, const uint16_
 // Router, top-k, permutation and control for one layer.
 void route_layer(ft_moe *h, int layer, const uint16_t *x, int T, bool decode,
                  const uint16_t *buffer, cudaStream_t s) {
-  launch_router(x, h->wr + (size_t)layer * h->E * h->d,
-                h->has_bias[layer] ? h->bias + (size_t)layer * h->E : nullptr, h->logits, T, h->E,
-                h->d, s);
-  launch_topk(h->logits, h->idx, h->w, h->tie, T, h->E, h->k, s);
+  {
+    ProfScope p(h, FT_PROF_ROUTER, s);
+    launch_router(x, h->wr + (size_t)layer * h->E * h->d,
+                  h->has_bias[layer] ? h->bias + (size_t)layer * h->E : nullptr, h->logits, T,
+                  h->E, h->d, s);
+  }
+  {
+    ProfScope p(h, FT_PROF_TOPK, s);
+    launch_topk(h->logits, h->idx, h->w, h->tie, T, h->E, h->k, s);
+  }
   ControlArgs a = control_args(h, layer, T, decode, buffer);
+  ProfScope p(h, FT_PROF_CONTROL, s);
   if (a.P > kPermSingleMax) {
     launch_perm_multi(a, h->chunk, s);
     launch_control(a, true, s);
@@ -194,15 +250,30 @@ void experts_layer(ft_moe *h, const uint16_t *x, int T, uint16_t *out, cudaStrea
   const int P = T * h->k;
   const int max_work = std::min(h->E, P) + h->n_shared;
   if (T <= kGemvMaxTokens) {
-    launch_gateup_gemv(h->work, h->ctr, max_work, x, h->tok, h->hbuf, T, h->d, h->d_ff, s);
+    {
+      ProfScope p(h, FT_PROF_GATEUP, s);
+      launch_gateup_gemv(h->work, h->ctr, max_work, x, h->tok, h->hbuf, T, h->d, h->d_ff, s);
+    }
+    ProfScope p(h, FT_PROF_DOWN, s);
     launch_down_gemv(h->work, h->ctr, max_work, h->hbuf, h->tok, h->wq, out, T, h->d, h->d_ff,
                      s);
   } else {
     const int rows = P + (h->n_shared ? T : 0);
-    launch_gather_rows(x, h->tok, h->xp, rows, h->d, s);
-    cudaMemsetAsync(h->acc, 0, (size_t)T * h->d * sizeof(float), s);
-    launch_gemm_ffn(h->work, h->ctr, max_work, T, h->xp, h->hbuf, h->tok, h->wq, h->acc, h->d,
-                    h->d_ff, s);
+    {
+      ProfScope p(h, FT_PROF_OTHER, s);
+      launch_gather_rows(x, h->tok, h->xp, rows, h->d, s);
+      cudaMemsetAsync(h->acc, 0, (size_t)T * h->d * sizeof(float), s);
+    }
+    {
+      ProfScope p(h, FT_PROF_GATEUP, s);
+      launch_gemm_gateup(h->work, h->ctr, max_work, T, h->xp, h->hbuf, h->d, h->d_ff, s);
+    }
+    {
+      ProfScope p(h, FT_PROF_DOWN, s);
+      launch_gemm_down(h->work, h->ctr, max_work, T, h->hbuf, h->tok, h->wq, h->acc, h->d,
+                       h->d_ff, s);
+    }
+    ProfScope p(h, FT_PROF_OTHER, s);
     launch_cast_out(h->acc, out, (size_t)T * h->d, h->ctr, s);
   }
 }
@@ -430,8 +501,11 @@ int ft_moe_forward(ft_moe *h, int layer, const void *x, int T, void *out, ft_str
   cudaStream_t s = (cudaStream_t)stream;
   const uint16_t *xb = static_cast<const uint16_t *>(x);
   route_layer(h, layer, xb, T, true, nullptr, s);
-  launch_fill(h->pool_dev, h->slots, h->fills, h->ctr, h->entry_bytes, h->E,
-              std::min(h->E, T * h->k), s);
+  {
+    ProfScope p(h, FT_PROF_FILL, s);
+    launch_fill(h->pool_dev, h->slots, h->fills, h->ctr, h->entry_bytes, h->E,
+                std::min(h->E, T * h->k), s);
+  }
   experts_layer(h, xb, T, static_cast<uint16_t *>(out), s);
   h->last_T = T;
   h->last_stream = s;
@@ -733,6 +807,27 @@ int ft_moe_get_fills(ft_moe *h, int32_t *n_fill, int32_t *fills, int cap) {
   if (fills && c.n_fill > 0) {
     const int n = std::min(cap, c.n_fill);
     FT_CUDA(cudaMemcpy(fills, h->fills, (size_t)n * 3 * 4, cudaMemcpyDeviceToHost));
+  }
+  return FT_OK;
+}
+
+int ft_moe_profile(ft_moe *h, int enable) {
+  if (int r = check_handle(h)) return r;
+  if (enable && (capturing(h->last_stream) || capturing(cudaStreamLegacy)))
+    return fail(FT_ERR_STATE, "profiling cannot be enabled during stream capture");
+  if (!enable) prof_flush(h);
+  h->prof_on = enable != 0;
+  return FT_OK;
+}
+
+int ft_moe_profile_read(ft_moe *h, double *ms, int64_t *launches) {
+  if (int r = check_handle(h)) return r;
+  prof_flush(h);
+  for (int i = 0; i < FT_PROF_N; ++i) {
+    if (ms) ms[i] += h->prof_ms[i];
+    if (launches) launches[i] += h->prof_n[i];
+    h->prof_ms[i] = 0;
+    h->prof_n[i] = 0;
   }
   return FT_OK;
 }

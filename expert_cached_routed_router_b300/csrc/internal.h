@@ -41,9 +41,11 @@ void launch_down_gemv(const WorkItem *work, const DevCounters *ctr, int max_work
 // Grouped-GEMM expert FFN for larger T.
 void launch_gather_rows(const uint16_t *x, const int32_t *tok, uint16_t *xp, int rows, int d,
                         cudaStream_t s);
-void launch_gemm_ffn(const WorkItem *work, const DevCounters *ctr, int max_work, int max_rows,
-                     const uint16_t *xp, uint16_t *h, const int32_t *tok, const float *wq,
-                     float *acc, int d, int d_ff, cudaStream_t s);
+void launch_gemm_gateup(const WorkItem *work, const DevCounters *ctr, int max_work, int max_rows,
+                        const uint16_t *xp, uint16_t *h, int d, int d_ff, cudaStream_t s);
+void launch_gemm_down(const WorkItem *work, const DevCounters *ctr, int max_work, int max_rows,
+                      const uint16_t *h, const int32_t *tok, const float *wq, float *acc, int d,
+                      int d_ff, cudaStream_t s);
 void launch_cast_out(const float *acc, uint16_t *out, size_t n, const DevCounters *ctr,
                      cudaStream_t s);
 

@@ -3,7 +3,7 @@
 This module draws random numbers and lays them out; it holds none of the layer's
 arithmetic (no router, no top-k, no FFN, no cache policy).
 
-Generator definition (the same on the host here and in ``synth.cu`` on the GPU):
+Generator definition (the same on the host here and in ``synth.cu`` on the GPU, bit for bit):
 
 * ``mix64`` is the splitmix64 output function (Steele, Lea and Flood, "Fast splittable
   pseudorandom number generators", OOPSLA 2014; the finaliser constants are
@@ -12,10 +12,14 @@ Generator definition (the same on the host here and in ``synth.cu`` on the GPU):
   with ``G = 0x9E3779B97F4A7C15`` (the splitmix64 increment), i.e. the i-th draw of a
   splitmix64 generator seeded with ``key``: counter based, so any element is
   computable on its own.
-* Normals use Box and Muller (1958): pair ``m`` takes ``u1 = ((s(2m) >> 11) + 1) * 2^-53``
-  in (0, 1] and ``u2 = (s(2m+1) >> 11) * 2^-53`` in [0, 1); ``r = sqrt(-2 ln u1)``,
-  ``z[2m] = r cos(2 pi u2)``, ``z[2m+1] = r sin(2 pi u2)``, all in double.
-* A value ``sigma * z`` is rounded double -> fp32 -> bf16 (round to nearest even).
+* Normal variates use the Irwin-Hall sum of 12 uniforms (the classical "sum of twelve
+  uniforms minus six" approximation): variate ``i`` takes draws 3i, 3i+1, 3i+2, splits
+  each into four 16-bit fields u_j, and returns ``z = (sum_j u_j - 393210) / 65536``, i.e.
+  ``sum_j (u_j + 1/2)/65536 - 6``.  Mean 0, variance 1 - 2^-32, excess kurtosis -0.1,
+  support [-6, 6].  Integer sums make it exact (z is an fp32 value), so the host and the
+  GPU produce identical bits without any transcendental function.
+* A value ``sigma * z`` is one fp32 multiply (sigma rounded to fp32 first), then bf16
+  (round to nearest even).  For sigma = 1 the value is bf16(z).
 
 bf16 tensors are returned as ``numpy.uint16`` bit patterns.
 """
@@ -26,7 +30,6 @@ import numpy as np
 G = np.uint64(0x9E3779B97F4A7C15)
 _M1 = np.uint64(0xBF58476D1CE4E5B9)
 _M2 = np.uint64(0x94D049BB133111EB)
-_TWO_M53 = 2.0 ** -53
 
 # Stream tags: which tensor a key belongs to.
 TAG_X = 1          # activations
@@ -65,20 +68,14 @@ def draws(key: int, start: int, n: int) -> np.ndarray:
         return mix64(np.uint64(key) + i * G)
 
 
-def normal_f64(key: int, n: int, start: int = 0) -> np.ndarray:
-    """Standard normals z[start .. start+n-1] of stream ``key`` (Box-Muller, double)."""
-    m0 = start // 2
-    m1 = (start + n + 1) // 2
-    s = draws(key, 2 * m0, 2 * (m1 - m0))
-    u1 = ((s[0::2] >> np.uint64(11)).astype(np.float64) + 1.0) * _TWO_M53
-    u2 = (s[1::2] >> np.uint64(11)).astype(np.float64) * _TWO_M53
-    r = np.sqrt(-2.0 * np.log(u1))
-    t = 2.0 * np.pi * u2
-    z = np.empty(2 * (m1 - m0), dtype=np.float64)
-    z[0::2] = r * np.cos(t)
-    z[1::2] = r * np.sin(t)
-    off = start - 2 * m0
-    return z[off:off + n]
+def normal_f32(key: int, n: int, start: int = 0) -> np.ndarray:
+    """Irwin-Hall normals z[start .. start+n-1] of stream ``key`` (exact fp32 values)."""
+    s = draws(key, 3 * start, 3 * n).reshape(n, 3)
+    tot = np.zeros(n, dtype=np.int64)
+    for j in range(3):
+        for f in range(4):
+            tot += ((s[:, j] >> np.uint64(16 * f)) & np.uint64(0xFFFF)).astype(np.int64)
+    return ((tot - 393210).astype(np.float32) / np.float32(65536.0)).astype(np.float32)
 
 
 def f32_to_bf16_bits(a) -> np.ndarray:
@@ -94,9 +91,11 @@ def bf16_bits_to_f32(b) -> np.ndarray:
 
 
 def normal_bf16(key: int, n: int, sigma: float, start: int = 0) -> np.ndarray:
-    """sigma * z rounded double -> fp32 -> bf16, as uint16 bits."""
-    v = (sigma * normal_f64(key, n, start)).astype(np.float32)
-    return f32_to_bf16_bits(v)
+    """bf16(fp32(sigma) * z) as uint16 bits (one fp32 multiply, then round to nearest even)."""
+    z = normal_f32(key, n, start)
+    if sigma != 1.0:
+        z = np.float32(sigma) * z
+    return f32_to_bf16_bits(z)
 
 
 # ---------------------------------------------------------------------------
@@ -114,8 +113,8 @@ def expert_entry(seed: int, layer: int, expert: int, d: int, d_ff: int,
 
     Layout of one entry (row-major, every row contiguous over its input features):
     ``Wg[d_ff][d]`` (row j holds W_gate[:, j]), ``Wu[d_ff][d]``, ``Wd[d][d_ff]``
-    (row i holds W_down[:, i]).  Element values are i.i.d. N(0, 0.02^2), so the
-    orientation changes no statistic.
+    (row i holds W_down[:, i]).  Element values are i.i.d. approximately N(0, 0.02^2), so
+    the orientation changes no statistic.
     """
     n = entry_elems(d, d_ff) - start if n is None else n
     return normal_bf16(stream_key(seed, TAG_POOL, layer, expert), n, ENTRY_SIGMA, start)
@@ -182,8 +181,8 @@ class DriftingZipfBias:
         """Advance the walk to the next step."""
         self.t += 1
         for l in range(self.L):
-            self.r[l] += self.sigma_walk * normal_f64(
-                stream_key(self.seed, TAG_DRIFT, l, self.t), self.E)
+            self.r[l] += self.sigma_walk * normal_f32(
+                stream_key(self.seed, TAG_DRIFT, l, self.t), self.E).astype(np.float64)
 
     def bias(self, layer: int) -> np.ndarray:
         """fp32 [E] bias of ``layer`` at the current step."""

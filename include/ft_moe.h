@@ -203,6 +203,27 @@ int ft_moe_get_fills(ft_moe *h, int32_t *n_fill, int32_t *fills, int cap);
 /* Sizes of a handle: [L, E, k, d, d_ff, n_slots, max_tokens, n_shared]. */
 int ft_moe_get_dims(ft_moe *h, int32_t dims[8]);
 
+/*
+ * Kernel timing for roofline measurement.  While enabled, forward and prefill bracket every
+ * kernel launch with a pair of CUDA events on the launching stream (so the enabled calls
+ * must not be captured).  ft_moe_profile_read synchronises, adds the elapsed time and
+ * launch count of each kernel class to ms[] / launches[] (arrays of FT_PROF_N, zeroed by the
+ * caller) and clears the record.  Recording adds a few microseconds per launch; time the
+ * throughput with profiling off.
+ */
+enum {
+  FT_PROF_ROUTER = 0,   /* router logits                                   */
+  FT_PROF_TOPK = 1,     /* top-k + gates                                   */
+  FT_PROF_CONTROL = 2,  /* grouping by expert + LRU update / buffer mapping */
+  FT_PROF_FILL = 3,     /* miss fills over the host link                   */
+  FT_PROF_GATEUP = 4,   /* gate/up + SwiGLU (GEMV or grouped GEMM)         */
+  FT_PROF_DOWN = 5,     /* down projection + weighted combine              */
+  FT_PROF_OTHER = 6,    /* gather, clear, cast                             */
+  FT_PROF_N = 7
+};
+int ft_moe_profile(ft_moe *h, int enable);
+int ft_moe_profile_read(ft_moe *h, double *ms, int64_t *launches);
+
 #ifdef __cplusplus
 }
 #endif

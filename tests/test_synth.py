@@ -12,15 +12,25 @@ def test_splitmix64_published_vectors():
 
 def test_counter_access_is_random_access():
     k = ft_synth.stream_key(0, ft_synth.TAG_POOL, 3, 5)
-    full = ft_synth.normal_f64(k, 101)
+    full = ft_synth.normal_f32(k, 101)
     for s, n in [(0, 1), (1, 1), (1, 6), (37, 20), (100, 1)]:
-        assert np.array_equal(ft_synth.normal_f64(k, n, start=s), full[s:s + n])
+        assert np.array_equal(ft_synth.normal_f32(k, n, start=s), full[s:s + n])
+
+
+def test_irwin_hall_by_hand():
+    """Variate 0 of a stream from its three draws, field by field."""
+    key = ft_synth.stream_key(0, ft_synth.TAG_X, 9)
+    d = [int(v) for v in ft_synth.draws(key, 0, 3)]
+    tot = sum((v >> (16 * f)) & 0xFFFF for v in d for f in range(4))
+    assert float(ft_synth.normal_f32(key, 1)[0]) == (tot - 393210) / 65536.0
 
 
 def test_normal_moments():
-    z = ft_synth.normal_f64(ft_synth.stream_key(0, ft_synth.TAG_X, 0), 400_000)
+    """Irwin-Hall(12): mean 0, variance 1 - 2^-32, kurtosis 3 - 6/60 = 2.9, |z| <= 6."""
+    z = ft_synth.normal_f32(ft_synth.stream_key(0, ft_synth.TAG_X, 0), 400_000).astype(np.float64)
     assert abs(z.mean()) < 0.01 and abs(z.std() - 1) < 0.01
-    assert abs(np.mean(z ** 4) - 3) < 0.05
+    assert abs(np.mean(z ** 4) - 2.9) < 0.05
+    assert np.abs(z).max() <= 6.0
 
 
 def test_bf16_round_to_nearest_even():
