@@ -27,7 +27,7 @@ EXPORTS = [
     "ft_moe_decode_host", "ft_moe_prefill_stream", "ft_moe_prefill_timing", "ft_cache_resize",
     "ft_cache_stats", "ft_cache_stats_reset", "ft_moe_status", "ft_moe_get_routing",
     "ft_moe_get_logits", "ft_moe_get_perm", "ft_moe_get_cache_state", "ft_moe_get_fills",
-    "ft_moe_get_dims", "ft_moe_profile", "ft_moe_profile_read",
+    "ft_moe_get_dims", "ft_moe_profile", "ft_moe_profile_read", "ft_route_topk_noalloc",
 ]
 
 PROF_CLASSES = ["router", "topk", "control", "fill", "gateup", "down", "other"]
@@ -96,6 +96,7 @@ def load_library(path: str = LIB_PATH):
         "ft_moe_get_dims": (I, [P, P]),
         "ft_moe_profile": (I, [P, I]),
         "ft_moe_profile_read": (I, [P, P, P]),
+        "ft_route_topk_noalloc": (I, [P, P, P, I, I, I, I, P, P, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -269,6 +270,14 @@ def ft_moe_profile_read(h) -> dict:
     n = np.zeros(len(PROF_CLASSES), np.int64)
     _check(load_library().ft_moe_profile_read(h, ms.ctypes.data, n.ctypes.data))
     return {c: (float(ms[i]), int(n[i])) for i, c in enumerate(PROF_CLASSES)}
+
+
+def ft_route_topk_noalloc(x, wr, bias, T, E, d, k, idx, w, tie, stream=None):
+    """Routing for callers that cannot allocate device memory: the caller passes every input
+    and output as device memory; the library keeps its scratch in a fixed device array."""
+    _check(load_library().ft_route_topk_noalloc(_ptr(x), _ptr(wr), _ptr(bias), T, E, d, k,
+                                                _ptr(idx), _ptr(w), _ptr(tie),
+                                                _stream(stream)))
 
 
 class MoELayerStack:

@@ -46,6 +46,11 @@ bool inject(const char *what) {
 
 }  // namespace
 
+int ftm::report_error(int code, const char *what, cudaError_t e) {
+  if (e != cudaSuccess) return fail(code, "%s: %s", what, cudaGetErrorString(e));
+  return fail(code, "%s", what);
+}
+
 struct ft_moe {
   int L = 0, E = 0, k = 0, d = 0, d_ff = 0, n_slots = 0, max_tokens = 0, n_shared = 0;
   int prewarm = 1, debug = 0;

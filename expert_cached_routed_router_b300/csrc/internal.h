@@ -49,4 +49,8 @@ void launch_gemm_down(const WorkItem *work, const DevCounters *ctr, int max_work
 void launch_cast_out(const float *acc, uint16_t *out, size_t n, const DevCounters *ctr,
                      cudaStream_t s);
 
+// Record `code` and a message (with the CUDA error string if e != cudaSuccess) as this
+// thread's ft_last_error(); returns code.
+int report_error(int code, const char *what, cudaError_t e);
+
 }  // namespace ftm

@@ -224,6 +224,27 @@ enum {
 int ft_moe_profile(ft_moe *h, int enable);
 int ft_moe_profile_read(ft_moe *h, double *ms, int64_t *launches);
 
+/*
+ * Routing that allocates nothing.  No counterpart in the paper (the FreeToken pages): it is a
+ * deployment aid for callers that cannot allocate device memory - code running while a
+ * global-mode stream capture is open (cudaMalloc is refused there), serving loops that must
+ * not pay for an allocation, and hosts whose framework owns all device memory.
+ *
+ * Computes, for one layer, what ft_moe_forward computes first: router logits in the same
+ * fixed fp32 order, top-k by (logit descending, expert id ascending), gates (softmax over the
+ * k selected logits) and near-tie flags.  Inputs: x = device bf16 [T][d], Wr = device bf16
+ * [E][d] (both 16-byte aligned), bias = device fp32 [E] or NULL.  Outputs (device, caller
+ * owned): idx int32 [T][k], w fp32 [T][k], tie uint8 [T].  Enqueued on `stream`.
+ * Limits: 1 <= k <= E <= 1024, k <= 32, d a multiple of 8, and T*E <= 262144; larger sizes
+ * return FT_ERR_INVALID.  The logits live in a fixed 1 MiB device array inside this library
+ * that every GPU using the library keeps until the process exits.  The first call on each
+ * device looks up that array's device address (with the device current), so make the first
+ * call before any stream capture.  All calls share the array: calls that overlap on the GPU
+ * race and must be ordered by the caller.
+ */
+int ft_route_topk_noalloc(const void *x, const void *Wr, const float *bias, int T, int E, int d,
+                          int k, int32_t *idx, float *w, uint8_t *tie, ft_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
