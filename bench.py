@@ -249,29 +249,43 @@ def bench_decode_batch(wl, pool, b, W, K, seed, world):
 
 
 def profile_decode_batch(wl, pool, b, x_all, bias_all, W, K, seed):
-    """Per-kernel device time over the same trace steps (events around each launch)."""
+    """Per-kernel device time over the same trace steps: the decode step is captured into a
+    CUDA graph with an event-record node before and after every kernel, replayed step by step."""
     import torch
-    from expert_cached_routed_router_b300 import PROF_CLASSES
-    L = wl["L"]
+    L, d = wl["L"], wl["d"]
     st = make_stack(wl, pool, seed, max_tokens=max(16, b))
-    out = torch.empty((L, b, wl["d"]), dtype=torch.int16, device="cuda")
-    for t in range(W):
-        st.set_router_bias(-1, bias_all[t])
+    xs = torch.empty((b, d), dtype=torch.int16, device="cuda")
+    bs = torch.empty((L, wl["E"]), dtype=torch.float32, device="cuda")
+    out = torch.empty((L, b, d), dtype=torch.int16, device="cuda")
+    st.profile(2)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        st.set_router_bias(-1, bs)
         for l in range(L):
-            st.forward(l, x_all[t], out[l])
+            st.forward(l, xs, out[l])
     torch.cuda.synchronize()
-    s0 = st.stats()
-    st.profile(True)
+
+    def run(t):
+        xs.copy_(x_all[t])
+        bs.copy_(bias_all[t])
+        g.replay()
+
+    for t in range(W):
+        run(t)
+    torch.cuda.synchronize()
     st.profile_read()
+    s0 = st.stats()
+    from expert_cached_routed_router_b300 import PROF_CLASSES
+    prof = {c: (0.0, 0) for c in PROF_CLASSES}
     for t in range(W, W + K):
-        st.set_router_bias(-1, bias_all[t])
-        for l in range(L):
-            st.forward(l, x_all[t], out[l])
-    prof = st.profile_read()
-    st.profile(False)
+        run(t)
+        p = st.profile_read()
+        prof = {c: (prof[c][0] + p[c][0], prof[c][1] + p[c][1]) for c in PROF_CLASSES}
     s1 = st.stats()
+    st.profile(False)
     touched = (s1["hits"] - s0["hits"]) + (s1["misses"] - s0["misses"])
     fill_bytes = s1["fill_bytes"] - s0["fill_bytes"]
+    del g
     st.close()
     return prof, touched, fill_bytes, K * L
 
@@ -553,10 +567,18 @@ def main():
     ap.add_argument("--prefill-steps", type=int, default=2)
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--batches", default="", help="comma list of decode batch sizes")
+    ap.add_argument("--slots", type=int, default=0, help="override the slot count")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     wl = dict(WORKLOADS[args.workload])
+    if args.batches:
+        wl["batches"] = tuple(int(v) for v in args.batches.split(","))
+        if wl.get("headline_b") not in wl["batches"]:
+            wl["headline_b"] = wl["batches"][0]
+    if args.slots:
+        wl["n_slots"] = args.slots
     import torch
     if args.impl == "reference":
         rank = int(os.environ.get("RANK", "0"))

@@ -260,7 +260,8 @@ def ft_moe_get_fills(h, cap=1024):
 
 
 def ft_moe_profile(h, enable):
-    _check(load_library().ft_moe_profile(h, 1 if enable else 0))
+    """enable: 0 off, 1 eager calls (True), 2 graph mode (events become graph nodes)."""
+    _check(load_library().ft_moe_profile(h, int(enable)))
 
 
 def ft_moe_profile_read(h) -> dict:

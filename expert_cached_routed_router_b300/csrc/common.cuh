@@ -22,7 +22,8 @@ struct DevCounters {
   int n_work;                    // work items of the most recent call
   int occupied;                  // slots holding an entry
   int call_status;               // 0, or FT_ERR_CAPACITY if the current call was refused
-  int pad[3];
+  unsigned route_arrive;         // CTAs of the fused routing kernel that have finished
+  int pad[2];
 };
 
 // One group of rows of the expert FFN: the rows q0 .. q0+count-1 of the permuted
@@ -41,6 +42,7 @@ struct ControlArgs {
   const float *w;       // [T][k]
   const uint8_t *tie;   // [T]
   int T, k, E, P;       // P = T*k
+  int d;                // hidden size (fused decode routing)
   int layer, L;
   int32_t *counts;      // [E]
   int32_t *offsets;     // [E+1]
@@ -77,12 +79,14 @@ __device__ __forceinline__ void set_status(DevCounters *c, int code) {
   atomicCAS(&c->status, 0, code);
 }
 
-// Streaming 16-byte load that bypasses L1 allocation (weights are read once).
+// Streaming 16-byte load that bypasses L1 allocation (weights are read once).  Not volatile:
+// the data is read-only for the kernel's lifetime, so the compiler may hoist these loads and
+// keep many in flight.
 __device__ __forceinline__ uint4 ld_stream(const void *p) {
   uint4 r;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-               : "l"(p));
+  asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+      : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+      : "l"(p));
   return r;
 }
 

@@ -12,8 +12,11 @@
 #include <stdint.h>
 
 #include <algorithm>
+#include <map>
+#include <mutex>
 
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace ftm {
 
@@ -58,153 +61,349 @@ void launch_fill(const uint16_t *pool_dev, uint16_t *slots, const int32_t *fills
 }
 
 // ---------------------------------------------------------------------------------------
-// Decode gate/up GEMV + SwiGLU.  CTA (feature block, work item): 8 warps, one output
-// feature j per warp; the warp streams W_gate row j and W_up row j once (16-byte loads,
-// 8 per lane in flight per row) and dots them with the item's <= 16 token rows staged in
-// shared memory.  h[q][j] = silu(g) * u, rounded to bf16.
+// Decode GEMVs fed by bulk TMA copies.
+//
+// One persistent CTA per SM: warp 8 is the producer, warps 0..7 consume.  Work is a list of
+// tasks (work item u, block of R consecutive weight rows); the rows of a block are contiguous
+// in the entry, so the producer moves each block with one cp.async.bulk per matrix into a ring
+// of kStages shared-memory stages (mbarrier "full" with transaction bytes, "empty" with one
+// arrival per consumer warp).  Bytes in flight per SM are kStages stages, independent of
+// registers.  Consumers dot the rows with the item's token vectors from shared memory.
+// All waits are bounded; on a timeout the CTA records FT_ERR_TIMEOUT, waits (bounded) for its
+// own copies in flight and returns.
 // ---------------------------------------------------------------------------------------
-constexpr int kGemvWarps = 8;
-constexpr int kNB = 8;  // 16-byte chunks per lane per row per batch
+constexpr int kGemvWarps = 8;            // consumer warps
+constexpr int kGemvThreads = (kGemvWarps + 1) * 32;
+constexpr int kMaxStages = 12;
+constexpr uint32_t kRingBytes = 192u << 10;  // all stages together
 
-template <int MAXT>
-__global__ void __launch_bounds__(kGemvWarps * 32) k_gateup_gemv(
-    const WorkItem *__restrict__ work, const DevCounters *__restrict__ ctr,
-    const uint16_t *__restrict__ x, const int32_t *__restrict__ tok, uint16_t *__restrict__ h,
-    int d, int d_ff) {
-  const int u = blockIdx.y;
-  if (u >= ctr->n_work) return;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int j = blockIdx.x * kGemvWarps + warp;
-  if (j >= d_ff) return;
-  const WorkItem wi = work[u];
-  const int c = min(wi.count, MAXT);
-  const int nchunk = d >> 3;
-  const uint4 *xr[MAXT];  // the item's token rows (read through L1: shared by the CTA's warps)
-#pragma unroll
-  for (int t = 0; t < MAXT; ++t)
-    xr[t] = reinterpret_cast<const uint4 *>(x + (size_t)(t < c ? tok[wi.q0 + t] : 0) * d);
-  const uint16_t *grow = wi.W + (size_t)j * d;
-  const uint16_t *urow = wi.W + (size_t)(d_ff + j) * d;
-  float ag[MAXT], au[MAXT];
-#pragma unroll
-  for (int t = 0; t < MAXT; ++t) ag[t] = au[t] = 0.f;
-  for (int cb = 0; cb < nchunk; cb += 32 * kNB) {
-    uint4 gv[kNB], uv[kNB];
-#pragma unroll
-    for (int b = 0; b < kNB; ++b) {
-      const int ch = cb + b * 32 + lane;
-      gv[b] = ch < nchunk ? ld_stream(grow + (size_t)ch * 8) : make_uint4(0, 0, 0, 0);
-      uv[b] = ch < nchunk ? ld_stream(urow + (size_t)ch * 8) : make_uint4(0, 0, 0, 0);
+// Stage size: 16 KB, or larger when one gate+up row pair (4*d bytes) or one W_down row needs it.
+static uint32_t stage_bytes_for(uint32_t min_bytes) {
+  uint32_t b = 16u << 10;
+  while (b < min_bytes) b <<= 1;
+  return b;
+}
+
+struct RingSmem {
+  uint8_t *base;
+  uint32_t stage_bytes;
+  int n;  // stages
+  uint64_t *full;
+  uint64_t *empty;
+  __device__ __forceinline__ uint8_t *stage(int s) const { return base + (size_t)s * stage_bytes; }
+};
+
+// Carve the dynamic shared memory: [x staging | stages | barriers].
+__device__ __forceinline__ RingSmem ring_layout(uint8_t *smem, size_t x_bytes, uint32_t stage_bytes) {
+  RingSmem r;
+  r.base = smem + ((x_bytes + 127) & ~(size_t)127);
+  r.stage_bytes = stage_bytes;
+  r.n = (int)min((uint32_t)kMaxStages, kRingBytes / stage_bytes);
+  r.full = reinterpret_cast<uint64_t *>(r.base + (size_t)r.n * stage_bytes);
+  r.empty = r.full + r.n;
+  return r;
+}
+
+static size_t ring_smem_bytes(size_t x_bytes, uint32_t stage_bytes) {
+  const int n = (int)std::min((uint32_t)kMaxStages, kRingBytes / stage_bytes);
+  return ((x_bytes + 127) & ~(size_t)127) + (size_t)n * stage_bytes + 2 * n * 8;
+}
+
+__device__ __forceinline__ void ring_init(RingSmem &r) {
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < r.n; ++s) {
+      mbar_init(&r.full[s], 1);
+      mbar_init(&r.empty[s], 1);
     }
+    fence_barrier_init();
+  }
+}
+
+// Producer side of the ring (one thread): for each of this CTA's tasks, wait for a free
+// stage and issue the bulk copies that `issue(task, stage_ptr, bar)` describes.  Returns
+// false on a timeout.  At the end it waits for its copies in flight.
+template <typename Issue>
+__device__ __forceinline__ bool ring_produce(RingSmem &r, long n_tasks, Issue issue) {
+  long it = 0;
+  bool ok = true;
+  for (long task = blockIdx.x; task < n_tasks; task += gridDim.x, ++it) {
+    const int s = (int)(it % r.n);
+    const uint32_t ph = (uint32_t)((it / r.n) & 1);
+    if (it >= r.n && !mbar_wait(&r.empty[s], ph ^ 1u)) {
+      ok = false;
+      break;
+    }
+    issue(task, r.stage(s), &r.full[s]);
+  }
+  // drain: the copies of the last min(it, n) tasks may still be in flight
+  for (long i = (it > r.n ? it - r.n : 0); i < it; ++i)
+    mbar_wait(&r.full[i % r.n], (uint32_t)((i / r.n) & 1));
+  return ok;
+}
+
+// Consumer side: consumer warp w takes this CTA's tasks w, w+8, ... whole; for each it waits
+// for the task's stage, runs `use`, and releases the stage.
+template <typename Use>
+__device__ __forceinline__ bool ring_consume(RingSmem &r, long n_tasks, Use use) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  long it = 0;
+  for (long task = blockIdx.x; task < n_tasks; task += gridDim.x, ++it) {
+    if ((int)(it % kGemvWarps) != warp) continue;
+    const int s = (int)(it % r.n);
+    const uint32_t ph = (uint32_t)((it / r.n) & 1);
+    if (!mbar_wait(&r.full[s], ph)) return false;
+    use(task, r.stage(s));
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&r.empty[s]);
+  }
+  return true;
+}
+
+// gate/up + SwiGLU.  Task = (item u, rows j0 .. j0+R-1 of W_gate and of W_up); stage =
+// [R gate rows | R up rows].  h[q][j] = silu(g) * u (bf16).
+template <int MAXT, bool XS>
+__global__ void __launch_bounds__(kGemvThreads, 1) k_gateup_tma(
+    const WorkItem *__restrict__ work, DevCounters *__restrict__ ctr,
+    const uint16_t *__restrict__ x, const int32_t *__restrict__ tok, uint16_t *__restrict__ h,
+    int T, int d, int d_ff, int R, uint32_t stage_bytes) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  if (ctr->call_status != 0) return;
+  const int n_work = ctr->n_work;
+  const int nchunk = d >> 3;
+  const size_t x_bytes = XS ? (size_t)T * d * 2 : 0;
+  RingSmem r = ring_layout(smem, x_bytes, stage_bytes);
+  const uint4 *xs = XS ? reinterpret_cast<const uint4 *>(smem) : reinterpret_cast<const uint4 *>(x);
+  if (XS)
+    for (int i = threadIdx.x; i < T * nchunk; i += blockDim.x)
+      reinterpret_cast<uint4 *>(smem)[i] = __ldg(reinterpret_cast<const uint4 *>(x) + i);
+  ring_init(r);
+  __syncthreads();
+  const int n_jb = (d_ff + R - 1) / R;
+  const long n_tasks = (long)n_work * n_jb;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  bool ok = true;
+  if (warp == kGemvWarps) {
+    if (lane == 0)
+      ok = ring_produce(r, n_tasks, [&](long task, uint8_t *st, uint64_t *bar) {
+        const int u = (int)(task / n_jb), j0 = (int)(task - (long)u * n_jb) * R;
+        const int rows = min(R, d_ff - j0);
+        const uint32_t bytes = (uint32_t)rows * d * 2;
+        const uint16_t *W = work[u].W;
+        mbar_arrive_expect_tx(bar, 2 * bytes);
+        bulk_g2s(st, W + (size_t)j0 * d, bytes, bar);
+        bulk_g2s(st + (size_t)R * d * 2, W + (size_t)(d_ff + j0) * d, bytes, bar);
+      });
+  } else {
+    ok = ring_consume(r, n_tasks, [&](long task, const uint8_t *st) {
+      const int u = (int)(task / n_jb), j0 = (int)(task - (long)u * n_jb) * R;
+      const int rows = min(R, d_ff - j0);
+      const WorkItem wi = work[u];
+      const int c = min(wi.count, MAXT);
+      int tk[MAXT];
 #pragma unroll
-    for (int b = 0; b < kNB; ++b) {
-      const int ch = cb + b * 32 + lane;
-      if (ch < nchunk) {
+      for (int t = 0; t < MAXT; ++t) tk[t] = (t < c) ? tok[wi.q0 + t] : 0;
+      for (int rr = 0; rr < rows; ++rr) {
+        const uint4 *g = reinterpret_cast<const uint4 *>(st + (size_t)rr * d * 2);
+        const uint4 *uu = reinterpret_cast<const uint4 *>(st + (size_t)(R + rr) * d * 2);
+        float ag[MAXT], au[MAXT];
+#pragma unroll
+        for (int t = 0; t < MAXT; ++t) ag[t] = au[t] = 0.f;
+        for (int ch = lane; ch < nchunk; ch += 32) {
+          const uint4 gv = g[ch], uv = uu[ch];
+#pragma unroll
+          for (int t = 0; t < MAXT; ++t) {
+            if (t < c) {
+              const uint4 xv = XS ? xs[tk[t] * nchunk + ch] : __ldg(xs + (size_t)tk[t] * nchunk + ch);
+              ag[t] = dot8_seq(gv, xv, ag[t]);
+              au[t] = dot8_seq(uv, xv, au[t]);
+            }
+          }
+        }
 #pragma unroll
         for (int t = 0; t < MAXT; ++t) {
           if (t < c) {
-            const uint4 xv = __ldg(xr[t] + ch);
-            ag[t] = dot8_seq(gv[b], xv, ag[t]);
-            au[t] = dot8_seq(uv[b], xv, au[t]);
+#pragma unroll
+            for (int off = 16; off >= 1; off >>= 1) {
+              ag[t] += __shfl_xor_sync(0xffffffffu, ag[t], off);
+              au[t] += __shfl_xor_sync(0xffffffffu, au[t], off);
+            }
+            if (lane == t)
+              h[(size_t)(wi.q0 + t) * d_ff + j0 + rr] = f32_to_bf16(silu_mul(ag[t], au[t]));
           }
         }
       }
-    }
+    });
   }
-#pragma unroll
-  for (int t = 0; t < MAXT; ++t) {
-    if (t < c) {
-#pragma unroll
-      for (int off = 16; off >= 1; off >>= 1) {
-        ag[t] += __shfl_xor_sync(0xffffffffu, ag[t], off);
-        au[t] += __shfl_xor_sync(0xffffffffu, au[t], off);
-      }
-      if (lane == t) h[(size_t)(wi.q0 + t) * d_ff + j] = f32_to_bf16(silu_mul(ag[t], au[t]));
-    }
-  }
+  if (!ok) set_status(ctr, FT_ERR_TIMEOUT);
 }
 
-void launch_gateup_gemv(const WorkItem *work, const DevCounters *ctr, int max_work,
-                        const uint16_t *x, const int32_t *tok, uint16_t *h, int T, int d,
-                        int d_ff, cudaStream_t s) {
-  dim3 grid((d_ff + kGemvWarps - 1) / kGemvWarps, max_work);
-  if (T <= 1)
-    k_gateup_gemv<1><<<grid, kGemvWarps * 32, 0, s>>>(work, ctr, x, tok, h, d, d_ff);
-  else if (T <= 4)
-    k_gateup_gemv<4><<<grid, kGemvWarps * 32, 0, s>>>(work, ctr, x, tok, h, d, d_ff);
-  else
-    k_gateup_gemv<16><<<grid, kGemvWarps * 32, 0, s>>>(work, ctr, x, tok, h, d, d_ff);
-}
-
-// ---------------------------------------------------------------------------------------
-// Decode down GEMV fused with the weighted combine.  One warp per output feature i: for
-// every work item (ascending expert id, then the shared expert) it streams W_down row i,
-// dots it with the item's h rows and adds w[q] * y into the accumulator of token tok[q],
-// which lane tok[q] holds.  The sum over a token's experts therefore runs in a fixed order
-// and the result is deterministic; out[t][i] = bf16(acc).
-// ---------------------------------------------------------------------------------------
+// down: task = (item u, rows i0 .. i0+R-1 of W_down); y[q][i] fp32 for the item's rows q.
 template <int MAXT>
-__global__ void __launch_bounds__(kGemvWarps * 32) k_down_gemv(
-    const WorkItem *__restrict__ work, const DevCounters *__restrict__ ctr,
-    const uint16_t *__restrict__ h, const int32_t *__restrict__ tok, const float *__restrict__ wq,
-    uint16_t *__restrict__ out, int T, int d, int d_ff) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int i = blockIdx.x * kGemvWarps + warp;
-  if (i >= d) return;
+__global__ void __launch_bounds__(kGemvThreads, 1) k_down_tma(
+    const WorkItem *__restrict__ work, DevCounters *__restrict__ ctr,
+    const uint16_t *__restrict__ h, float *__restrict__ y, int d, int d_ff, int R,
+    uint32_t stage_bytes) {
+  extern __shared__ __align__(128) uint8_t smem[];
   if (ctr->call_status != 0) return;
   const int n_work = ctr->n_work;
   const int nchunk = d_ff >> 3;
-  float acc = 0.f;
-  for (int u = 0; u < n_work; ++u) {
-    const WorkItem wi = work[u];
-    const uint16_t *row = wi.W + (size_t)2 * d_ff * d + (size_t)i * d_ff;
-    const int c = min(wi.count, MAXT);
-    float part[MAXT];
+  RingSmem r = ring_layout(smem, 0, stage_bytes);
+  ring_init(r);
+  __syncthreads();
+  const int n_ib = (d + R - 1) / R;
+  const long n_tasks = (long)n_work * n_ib;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  bool ok = true;
+  if (warp == kGemvWarps) {
+    if (lane == 0)
+      ok = ring_produce(r, n_tasks, [&](long task, uint8_t *st, uint64_t *bar) {
+        const int u = (int)(task / n_ib), i0 = (int)(task - (long)u * n_ib) * R;
+        const int rows = min(R, d - i0);
+        const uint32_t bytes = (uint32_t)rows * d_ff * 2;
+        mbar_arrive_expect_tx(bar, bytes);
+        bulk_g2s(st, work[u].W + (size_t)2 * d_ff * d + (size_t)i0 * d_ff, bytes, bar);
+      });
+  } else {
+    ok = ring_consume(r, n_tasks, [&](long task, const uint8_t *st) {
+      const int u = (int)(task / n_ib), i0 = (int)(task - (long)u * n_ib) * R;
+      const int rows = min(R, d - i0);
+      const WorkItem wi = work[u];
+      const int c = min(wi.count, MAXT);
+      for (int rr = 0; rr < rows; ++rr) {
+        const uint4 *wrow = reinterpret_cast<const uint4 *>(st + (size_t)rr * d_ff * 2);
+        float part[MAXT];
 #pragma unroll
-    for (int r = 0; r < MAXT; ++r) part[r] = 0.f;
-    for (int cb = 0; cb < nchunk; cb += 32 * kNB) {
-      uint4 wv[kNB];
+        for (int t = 0; t < MAXT; ++t) part[t] = 0.f;
+        for (int ch = lane; ch < nchunk; ch += 32) {
+          const uint4 wv = wrow[ch];
 #pragma unroll
-      for (int b = 0; b < kNB; ++b) {
-        const int ch = cb + b * 32 + lane;
-        wv[b] = ch < nchunk ? ld_stream(row + (size_t)ch * 8) : make_uint4(0, 0, 0, 0);
-      }
+          for (int t = 0; t < MAXT; ++t)
+            if (t < c)
+              part[t] = dot8_seq(
+                  wv, __ldg(reinterpret_cast<const uint4 *>(h + (size_t)(wi.q0 + t) * d_ff) + ch),
+                  part[t]);
+        }
 #pragma unroll
-      for (int r = 0; r < MAXT; ++r) {
-        if (r < c) {
-          const uint4 *hr = reinterpret_cast<const uint4 *>(h + (size_t)(wi.q0 + r) * d_ff);
+        for (int t = 0; t < MAXT; ++t) {
+          if (t < c) {
 #pragma unroll
-          for (int b = 0; b < kNB; ++b) {
-            const int ch = cb + b * 32 + lane;
-            if (ch < nchunk) part[r] = dot8_seq(wv[b], __ldg(hr + ch), part[r]);
+            for (int off = 16; off >= 1; off >>= 1) part[t] += __shfl_xor_sync(0xffffffffu, part[t], off);
+            if (lane == t) y[(size_t)(wi.q0 + t) * d + i0 + rr] = part[t];
           }
         }
       }
-    }
-#pragma unroll
-    for (int r = 0; r < MAXT; ++r) {
-      if (r < c) {
-#pragma unroll
-        for (int off = 16; off >= 1; off >>= 1) part[r] += __shfl_xor_sync(0xffffffffu, part[r], off);
-        const int q = wi.q0 + r;
-        if (lane == tok[q]) acc = fmaf(wq[q], part[r], acc);
-      }
-    }
+    });
   }
-  if (lane < T) out[(size_t)lane * d + i] = f32_to_bf16(acc);
+  if (!ok) set_status(ctr, FT_ERR_TIMEOUT);
 }
 
-void launch_down_gemv(const WorkItem *work, const DevCounters *ctr, int max_work,
-                      const uint16_t *h, const int32_t *tok, const float *wq, uint16_t *out, int T,
-                      int d, int d_ff, cudaStream_t s) {
+static int sm_count() {
+  static int n = 0;
+  if (!n) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 148;
+  }
+  return n;
+}
+
+template <typename K>
+static void allow_smem(K kern, size_t smem) {
+  static std::mutex mu;
+  static std::map<const void *, size_t> done;
+  std::lock_guard<std::mutex> lock(mu);
+  size_t &v = done[reinterpret_cast<const void *>(kern)];
+  if (smem > v) {
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    v = smem;
+  }
+}
+
+void launch_gateup_gemv(const WorkItem *work, DevCounters *ctr, int max_work, const uint16_t *x,
+                        const int32_t *tok, uint16_t *h, int T, int d, int d_ff, cudaStream_t s) {
   (void)max_work;
-  dim3 grid((d + kGemvWarps - 1) / kGemvWarps);
+  const uint32_t sb = stage_bytes_for(4u * d);
+  const int R = std::max(1, std::min(d_ff, (int)(sb / (4u * d))));
+  const bool xs = (size_t)T * d * 2 <= (32u << 10);
+  const size_t smem = ring_smem_bytes(xs ? (size_t)T * d * 2 : 0, sb);
+  auto go = [&](auto kern) {
+    allow_smem(kern, smem);
+    kern<<<sm_count(), kGemvThreads, smem, s>>>(work, ctr, x, tok, h, T, d, d_ff, R, sb);
+  };
   if (T <= 1)
-    k_down_gemv<1><<<grid, kGemvWarps * 32, 0, s>>>(work, ctr, h, tok, wq, out, T, d, d_ff);
+    xs ? go(k_gateup_tma<1, true>) : go(k_gateup_tma<1, false>);
   else if (T <= 4)
-    k_down_gemv<4><<<grid, kGemvWarps * 32, 0, s>>>(work, ctr, h, tok, wq, out, T, d, d_ff);
+    xs ? go(k_gateup_tma<4, true>) : go(k_gateup_tma<4, false>);
   else
-    k_down_gemv<16><<<grid, kGemvWarps * 32, 0, s>>>(work, ctr, h, tok, wq, out, T, d, d_ff);
+    xs ? go(k_gateup_tma<16, true>) : go(k_gateup_tma<16, false>);
+}
+
+// out[t][i] = sum_j w[t][j] * y[inv[t*k+j]][i] (j ascending) + y[P+t][i] for the shared
+// expert; fixed order, so the result is deterministic.  8 features per thread.
+__global__ void k_combine(const float *__restrict__ y, const float *__restrict__ w,
+                          const int32_t *__restrict__ inv, const DevCounters *__restrict__ ctr,
+                          uint16_t *__restrict__ out, int T, int k, int d, int shared) {
+  if (ctr->call_status != 0) return;
+  const int n8 = d >> 3;
+  const int gidx = blockIdx.x * blockDim.x + threadIdx.x;
+  if (gidx >= T * n8) return;
+  const int t = gidx / n8, c = gidx - t * n8;
+  float acc[8];
+#pragma unroll
+  for (int v = 0; v < 8; ++v) acc[v] = 0.f;
+  for (int j = 0; j < k; ++j) {
+    const float wj = w[t * k + j];
+    const float4 *row = reinterpret_cast<const float4 *>(y + (size_t)inv[t * k + j] * d) + 2 * c;
+    const float4 a = row[0], b = row[1];
+    acc[0] = fmaf(wj, a.x, acc[0]);
+    acc[1] = fmaf(wj, a.y, acc[1]);
+    acc[2] = fmaf(wj, a.z, acc[2]);
+    acc[3] = fmaf(wj, a.w, acc[3]);
+    acc[4] = fmaf(wj, b.x, acc[4]);
+    acc[5] = fmaf(wj, b.y, acc[5]);
+    acc[6] = fmaf(wj, b.z, acc[6]);
+    acc[7] = fmaf(wj, b.w, acc[7]);
+  }
+  if (shared) {
+    const float4 *row = reinterpret_cast<const float4 *>(y + (size_t)(T * k + t) * d) + 2 * c;
+    const float4 a = row[0], b = row[1];
+    acc[0] += a.x;
+    acc[1] += a.y;
+    acc[2] += a.z;
+    acc[3] += a.w;
+    acc[4] += b.x;
+    acc[5] += b.y;
+    acc[6] += b.z;
+    acc[7] += b.w;
+  }
+  uint4 o;
+  o.x = (uint32_t)f32_to_bf16(acc[0]) | ((uint32_t)f32_to_bf16(acc[1]) << 16);
+  o.y = (uint32_t)f32_to_bf16(acc[2]) | ((uint32_t)f32_to_bf16(acc[3]) << 16);
+  o.z = (uint32_t)f32_to_bf16(acc[4]) | ((uint32_t)f32_to_bf16(acc[5]) << 16);
+  o.w = (uint32_t)f32_to_bf16(acc[6]) | ((uint32_t)f32_to_bf16(acc[7]) << 16);
+  reinterpret_cast<uint4 *>(out + (size_t)t * d)[c] = o;
+}
+
+void launch_down_gemv(const WorkItem *work, DevCounters *ctr, int max_work, const uint16_t *h,
+                      const int32_t *inv, const float *w, float *y, uint16_t *out, int T, int k,
+                      int d, int d_ff, int shared, cudaStream_t s) {
+  (void)max_work;
+  const uint32_t sb = stage_bytes_for(2u * d_ff);
+  const int R = std::max(1, std::min(d, (int)(sb / (2u * d_ff))));
+  const size_t smem = ring_smem_bytes(0, sb);
+  auto go = [&](auto kern) {
+    allow_smem(kern, smem);
+    kern<<<sm_count(), kGemvThreads, smem, s>>>(work, ctr, h, y, d, d_ff, R, sb);
+  };
+  if (T <= 1)
+    go(k_down_tma<1>);
+  else if (T <= 4)
+    go(k_down_tma<4>);
+  else
+    go(k_down_tma<16>);
+  const int n = T * (d >> 3);
+  k_combine<<<(n + 255) / 256, 256, 0, s>>>(y, w, inv, ctr, out, T, k, d, shared);
 }
 
 // ---------------------------------------------------------------------------------------
@@ -229,97 +428,6 @@ void launch_gather_rows(const uint16_t *x, const int32_t *tok, uint16_t *xp, int
   const int threads = 256;
   const unsigned blocks = (unsigned)std::min<size_t>((n + threads - 1) / threads, 148 * 16);
   k_gather_rows<<<blocks, threads, 0, s>>>(x, tok, xp, rows, d);
-}
-
-// CUDA-core tiled GEMM, 64 x 64 output tile, K step 32, 4 x 4 outputs per thread.
-// GATEUP: h[q][j] = silu(xp[q] . Wg[j]) * (xp[q] . Wu[j])          (K = d)
-// DOWN:   acc[tok[q]][i] += wq[q] * (h[q] . Wd[i])  (fp32 atomics)  (K = d_ff)
-constexpr int kTM = 64, kTN = 64, kTK = 32;
-
-template <bool GATEUP>
-__global__ void __launch_bounds__(256) k_gemm_simt(const WorkItem *__restrict__ work,
-                                                   const DevCounters *__restrict__ ctr,
-                                                   const uint16_t *__restrict__ A,
-                                                   uint16_t *__restrict__ h,
-                                                   const int32_t *__restrict__ tok,
-                                                   const float *__restrict__ wq,
-                                                   float *__restrict__ acc, int d, int d_ff) {
-  const int u = blockIdx.z;
-  if (u >= ctr->n_work) return;
-  if (ctr->call_status != 0) return;
-  const WorkItem wi = work[u];
-  const int m0 = blockIdx.y * kTM;
-  if (m0 >= wi.count) return;
-  const int n0 = blockIdx.x * kTN;
-  const int K = GATEUP ? d : d_ff;
-  const int Nout = GATEUP ? d_ff : d;
-  if (n0 >= Nout) return;
-  const uint16_t *B0 = GATEUP ? wi.W : wi.W + (size_t)2 * d_ff * d;  // rows [Nout][K]
-  const uint16_t *B1 = wi.W + (size_t)d_ff * d;                        // W_up rows (GATEUP)
-  __shared__ float As[kTK][kTM + 4];
-  __shared__ float Bs[kTK][kTN + 4];
-  __shared__ float Us[GATEUP ? kTK : 1][kTN + 4];
-  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
-  float cg[4][4] = {}, cu[4][4] = {};
-  for (int k0 = 0; k0 < K; k0 += kTK) {
-    for (int i = threadIdx.x; i < kTM * kTK; i += 256) {
-      const int r = i / kTK, kk = i % kTK;
-      const int m = m0 + r;
-      As[kk][r] = (m < wi.count) ? bf16_to_f32(A[(size_t)(wi.q0 + m) * K + k0 + kk]) : 0.f;
-      const int n = n0 + r;
-      Bs[kk][r] = (n < Nout) ? bf16_to_f32(B0[(size_t)n * K + k0 + kk]) : 0.f;
-      if (GATEUP) Us[kk][r] = (n < Nout) ? bf16_to_f32(B1[(size_t)n * K + k0 + kk]) : 0.f;
-    }
-    __syncthreads();
-#pragma unroll 8
-    for (int kk = 0; kk < kTK; ++kk) {
-      float a[4], b[4], bu[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        a[i] = As[kk][ty * 4 + i];
-        b[i] = Bs[kk][tx * 4 + i];
-        if (GATEUP) bu[i] = Us[kk][tx * 4 + i];
-      }
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          cg[i][j] = fmaf(a[i], b[j], cg[i][j]);
-          if (GATEUP) cu[i][j] = fmaf(a[i], bu[j], cu[i][j]);
-        }
-    }
-    __syncthreads();
-  }
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int m = m0 + ty * 4 + i;
-    if (m >= wi.count) continue;
-    const int q = wi.q0 + m;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int n = n0 + tx * 4 + j;
-      if (n >= Nout) continue;
-      if (GATEUP)
-        h[(size_t)q * d_ff + n] = f32_to_bf16(silu_mul(cg[i][j], cu[i][j]));
-      else
-        atomicAdd(&acc[(size_t)tok[q] * d + n], wq[q] * cg[i][j]);
-    }
-  }
-}
-
-void launch_gemm_gateup(const WorkItem *work, const DevCounters *ctr, int max_work, int max_rows,
-                        const uint16_t *xp, uint16_t *h, int d, int d_ff, cudaStream_t s) {
-  const unsigned my = (unsigned)((max_rows + kTM - 1) / kTM);
-  dim3 g1((d_ff + kTN - 1) / kTN, my, max_work);
-  k_gemm_simt<true><<<g1, 256, 0, s>>>(work, ctr, xp, h, nullptr, nullptr, nullptr, d, d_ff);
-}
-
-void launch_gemm_down(const WorkItem *work, const DevCounters *ctr, int max_work, int max_rows,
-                      const uint16_t *h, const int32_t *tok, const float *wq, float *acc, int d,
-                      int d_ff, cudaStream_t s) {
-  const unsigned my = (unsigned)((max_rows + kTM - 1) / kTM);
-  dim3 g2((d + kTN - 1) / kTN, my, max_work);
-  k_gemm_simt<false><<<g2, 256, 0, s>>>(work, ctr, h, nullptr, tok, wq, acc, d, d_ff);
 }
 
 __global__ void k_cast_out(const float *__restrict__ acc, uint16_t *__restrict__ out, size_t n,

@@ -79,7 +79,11 @@ struct ft_moe {
   uint16_t *hbuf = nullptr;
   uint16_t *xp = nullptr;
   float *acc = nullptr;
+  float *ybuf = nullptr;  // decode: fp32 rows of the down projection [(16k + 16)][d]
   int32_t *chunk = nullptr;
+  int *tile_prefix = nullptr;  // tcgen05 tile scheduler [kMaxE + 3]
+  TcMaps maps_slots{};         // tensor maps over the slot storage
+  TcMaps maps_dbuf[2]{};       // ... over the prefill double buffer
   uint64_t resizes = 0;
 
   // pool
@@ -104,6 +108,7 @@ struct ft_moe {
 
   // kernel timing (ft_moe_profile)
   bool prof_on = false;
+  bool prof_keep = false;                     // graph mode: keep the recorded pairs
   std::vector<cudaEvent_t> prof_events;       // pool; pairs (begin, end)
   std::vector<int> prof_class;                // class of pair i
   double prof_ms[FT_PROF_N] = {};
@@ -129,7 +134,8 @@ int alloc_n(ft_moe *h, T **p, size_t n) {
   return dev_alloc(h, reinterpret_cast<void **>(p), n * sizeof(T));
 }
 
-// Sum the recorded event pairs into prof_ms / prof_n and clear the record.
+// Sum the recorded event pairs into prof_ms / prof_n and clear the record (in graph mode
+// the pairs are kept: every replay of the captured graph records them again).
 void prof_flush(ft_moe *h) {
   if (h->prof_class.empty()) return;
   cudaEventSynchronize(h->prof_events[2 * h->prof_class.size() - 1]);
@@ -141,7 +147,7 @@ void prof_flush(ft_moe *h) {
     }
   }
   cudaGetLastError();
-  h->prof_class.clear();
+  if (!h->prof_keep) h->prof_class.clear();
 }
 
 // Brackets one kernel launch with timing events while profiling is on.
@@ -152,6 +158,7 @@ struct ProfScope {
   ProfScope(ft_moe *h_, int cls, cudaStream_t s_) : h(h_), s(s_) {
     if (!h->prof_on) return;
     if (2 * (h->prof_class.size() + 1) > h->prof_events.size()) {
+      if (h->prof_keep) return;  // graph mode: the pool was sized when profiling was enabled
       if (h->prof_events.size() < 16384) {
         for (int i = 0; i < 512; ++i) {
           cudaEvent_t e;
@@ -163,10 +170,17 @@ struct ProfScope {
     }
     idx = (int)h->prof_class.size();
     h->prof_class.push_back(cls);
-    cudaEventRecord(h->prof_events[2 * idx], s);
+    record(h->prof_events[2 * idx]);
   }
   ~ProfScope() {
-    if (idx >= 0) cudaEventRecord(h->prof_events[2 * idx + 1], s);
+    if (idx >= 0) record(h->prof_events[2 * idx + 1]);
+  }
+  // In graph mode the records are captured as external event nodes, which keep timing.
+  void record(cudaEvent_t e) {
+    if (h->prof_keep)
+      cudaEventRecordWithFlags(e, s, cudaEventRecordExternal);
+    else
+      cudaEventRecord(e, s);
   }
 };
 
@@ -224,12 +238,40 @@ ControlArgs control_args(ft_moe *h, int layer, int T, bool decode, const uint16_
   a.shared = h->n_shared ? h->shared + (size_t)layer * h->entry_elems : nullptr;
   a.entry_elems = h->entry_elems;
   a.ctr = h->ctr;
+  a.d = h->d;
   return a;
+}
+
+// Tensor maps for the tcgen05 GEMMs over `buffer` (n_entries complete entries).
+int build_maps(ft_moe *h, TcMaps *m, const uint16_t *buffer, int n_entries) {
+  const uint64_t R = (uint64_t)h->max_tokens * h->k + h->max_tokens;
+  const uint64_t d = h->d, f = h->d_ff;
+  const uint16_t *sh = h->shared ? h->shared : buffer;
+  const uint64_t nsh = h->shared ? (uint64_t)h->L : (uint64_t)n_entries;
+  bool ok = make_tmap(&m->a_x, h->xp, d, R, 128) && make_tmap(&m->a_h, h->hbuf, f, R, 128) &&
+            make_tmap(&m->b_gu, buffer, d, (uint64_t)n_entries * 3 * f, 128) &&
+            make_tmap(&m->bs_gu, sh, d, nsh * 3 * f, 128) &&
+            make_tmap(&m->b_dn128, buffer, f, (uint64_t)n_entries * 3 * d, 128) &&
+            make_tmap(&m->bs_dn128, sh, f, nsh * 3 * d, 128);
+  if (ok && d % 256 == 0)
+    ok = make_tmap(&m->b_dn256, buffer, f, (uint64_t)n_entries * 3 * d, 256) &&
+         make_tmap(&m->bs_dn256, sh, f, nsh * 3 * d, 256);
+  if (!ok) return fail(FT_ERR_CUDA, "cuTensorMapEncodeTiled failed");
+  return FT_OK;
 }
 
 // Router, top-k, permutation and control for one layer.
 void route_layer(ft_moe *h, int layer, const uint16_t *x, int T, bool decode,
                  const uint16_t *buffer, cudaStream_t s) {
+  if (decode && T <= kGemvMaxTokens) {
+    // router, top-k, grouping and the LRU update in one launch
+    ControlArgs a = control_args(h, layer, T, decode, buffer);
+    ProfScope p(h, FT_PROF_ROUTER, s);
+    launch_route_decode(x, h->wr + (size_t)layer * h->E * h->d,
+                        h->has_bias[layer] ? h->bias + (size_t)layer * h->E : nullptr, h->logits,
+                        a, s);
+    return;
+  }
   {
     ProfScope p(h, FT_PROF_ROUTER, s);
     launch_router(x, h->wr + (size_t)layer * h->E * h->d,
@@ -250,8 +292,9 @@ void route_layer(ft_moe *h, int layer, const uint16_t *x, int T, bool decode,
   }
 }
 
-// Expert FFN + combine for one layer after routing.
-void experts_layer(ft_moe *h, const uint16_t *x, int T, uint16_t *out, cudaStream_t s) {
+// Expert FFN + combine for one layer after routing; `maps` view the weights' buffer.
+void experts_layer(ft_moe *h, const uint16_t *x, int T, uint16_t *out, const TcMaps &maps,
+                   int layer, cudaStream_t s) {
   const int P = T * h->k;
   const int max_work = std::min(h->E, P) + h->n_shared;
   if (T <= kGemvMaxTokens) {
@@ -260,8 +303,8 @@ void experts_layer(ft_moe *h, const uint16_t *x, int T, uint16_t *out, cudaStrea
       launch_gateup_gemv(h->work, h->ctr, max_work, x, h->tok, h->hbuf, T, h->d, h->d_ff, s);
     }
     ProfScope p(h, FT_PROF_DOWN, s);
-    launch_down_gemv(h->work, h->ctr, max_work, h->hbuf, h->tok, h->wq, out, T, h->d, h->d_ff,
-                     s);
+    launch_down_gemv(h->work, h->ctr, max_work, h->hbuf, h->inv, h->w, h->ybuf, out, T, h->k,
+                     h->d, h->d_ff, h->n_shared, s);
   } else {
     const int rows = P + (h->n_shared ? T : 0);
     {
@@ -270,13 +313,9 @@ void experts_layer(ft_moe *h, const uint16_t *x, int T, uint16_t *out, cudaStrea
       cudaMemsetAsync(h->acc, 0, (size_t)T * h->d * sizeof(float), s);
     }
     {
-      ProfScope p(h, FT_PROF_GATEUP, s);
-      launch_gemm_gateup(h->work, h->ctr, max_work, T, h->xp, h->hbuf, h->d, h->d_ff, s);
-    }
-    {
-      ProfScope p(h, FT_PROF_DOWN, s);
-      launch_gemm_down(h->work, h->ctr, max_work, T, h->hbuf, h->tok, h->wq, h->acc, h->d,
-                       h->d_ff, s);
+      ProfScope p(h, FT_PROF_GATEUP, s);  // gate/up and down GEMMs on the tensor cores
+      launch_tc_ffn(maps, h->work, h->ctr, h->tile_prefix, h->hbuf, h->tok, h->wq, h->acc, h->d,
+                    h->d_ff, layer, s);
     }
     ProfScope p(h, FT_PROF_OTHER, s);
     launch_cast_out(h->acc, out, (size_t)T * h->d, h->ctr, s);
@@ -352,7 +391,9 @@ int ft_moe_create(int L, int E, int k, int d, int d_ff, int n_slots, const ft_mo
   A(alloc_n(h, &h->hbuf, R * d_ff));
   A(alloc_n(h, &h->xp, R * d));
   A(alloc_n(h, &h->acc, T * d));
+  A(alloc_n(h, &h->ybuf, (size_t)(kGemvMaxTokens * k + kGemvMaxTokens) * d));
   A(alloc_n(h, &h->chunk, perm_multi_scratch_ints((int)P, E)));
+  A(alloc_n(h, &h->tile_prefix, (size_t)kMaxE + 3));
   if (rc == FT_OK) {
     cudaError_t e = cudaMalloc(&h->slots, (size_t)n_slots * h->entry_bytes);
     if (e == cudaSuccess) e = cudaMalloc(&h->owner, (size_t)n_slots * sizeof(int32_t));
@@ -376,6 +417,7 @@ int ft_moe_create(int L, int E, int k, int d, int d_ff, int n_slots, const ft_mo
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (e != cudaSuccess) rc = fail(FT_ERR_CUDA, "initialisation: %s", cudaGetErrorString(e));
   }
+  if (rc == FT_OK) rc = build_maps(h, &h->maps_slots, h->slots, n_slots);
   if (rc != FT_OK) {
     free_all(h);
     delete h;
@@ -511,7 +553,7 @@ int ft_moe_forward(ft_moe *h, int layer, const void *x, int T, void *out, ft_str
     launch_fill(h->pool_dev, h->slots, h->fills, h->ctr, h->entry_bytes, h->E,
                 std::min(h->E, T * h->k), s);
   }
-  experts_layer(h, xb, T, static_cast<uint16_t *>(out), s);
+  experts_layer(h, xb, T, static_cast<uint16_t *>(out), h->maps_slots, layer, s);
   h->last_T = T;
   h->last_stream = s;
   cudaError_t e = cudaGetLastError();
@@ -579,6 +621,7 @@ int ft_moe_prefill_stream(ft_moe *h, int layer0, int n_layers, const void *x, in
         return fail(FT_ERR_OOM, "double buffer (%zu bytes): %s", layer_bytes,
                     cudaGetErrorString(e));
       }
+      if (int r = build_maps(h, &h->maps_dbuf[i], h->dbuf[i], h->E)) return r;
     }
   }
   while ((int)h->ev_cs.size() < n_layers) {
@@ -615,7 +658,7 @@ int ft_moe_prefill_stream(ft_moe *h, int layer0, int n_layers, const void *x, in
     FT_CUDA(cudaStreamWaitEvent(s, h->ev_ce[i], 0));
     FT_CUDA(cudaEventRecord(h->ev_ks[i], s));
     route_layer(h, layer0 + i, xb, T, false, h->dbuf[i & 1], s);
-    experts_layer(h, xb, T, ob + (size_t)i * T * h->d, s);
+    experts_layer(h, xb, T, ob + (size_t)i * T * h->d, h->maps_dbuf[i & 1], layer0 + i, s);
     FT_CUDA(cudaEventRecord(h->ev_ke[i], s));
   }
   h->last_prefill_layers = n_layers;
@@ -706,6 +749,7 @@ int ft_cache_resize(ft_moe *h, int n_new) {
   h->owner = nowner;
   h->stamps = nstamps;
   h->n_slots = n_new;
+  if (int r = build_maps(h, &h->maps_slots, h->slots, n_new)) return r;
   DevCounters c{};
   FT_CUDA(cudaMemcpy(&c, h->ctr, sizeof(c), cudaMemcpyDeviceToHost));
   c.occupied = m;
@@ -820,7 +864,21 @@ int ft_moe_profile(ft_moe *h, int enable) {
   if (int r = check_handle(h)) return r;
   if (enable && (capturing(h->last_stream) || capturing(cudaStreamLegacy)))
     return fail(FT_ERR_STATE, "profiling cannot be enabled during stream capture");
-  if (!enable) prof_flush(h);
+  if (!enable) {
+    h->prof_keep = false;
+    prof_flush(h);
+    h->prof_class.clear();
+  } else {
+    h->prof_class.clear();
+    if (enable == 2) {  // graph mode: events for up to 4096 launches, created now
+      while (h->prof_events.size() < 8192) {
+        cudaEvent_t e;
+        FT_CUDA(cudaEventCreate(&e));
+        h->prof_events.push_back(e);
+      }
+    }
+    h->prof_keep = enable == 2;
+  }
   h->prof_on = enable != 0;
   return FT_OK;
 }

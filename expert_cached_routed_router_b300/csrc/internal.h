@@ -1,6 +1,7 @@
 // Host-side launchers shared between the translation units of the ft_moe library.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -25,29 +26,40 @@ size_t perm_multi_scratch_ints(int P, int E);
 void launch_control(const ControlArgs &a, bool perm_ready, cudaStream_t s);
 constexpr int kPermSingleMax = 1024;  // largest P the single-CTA control permutes itself
 
+// Decode routing in one launch: router logits, then (last CTA) top-k + control.  T <= 16.
+void launch_route_decode(const uint16_t *x, const uint16_t *wr, const float *bias, float *logits,
+                         const ControlArgs &a, cudaStream_t s);
+
 // Copy the fill list's entries from the mapped host pool into their slots.
 void launch_fill(const uint16_t *pool_dev, uint16_t *slots, const int32_t *fills,
                  const DevCounters *ctr, size_t entry_bytes, int E, int max_fill, cudaStream_t s);
 
-// Decode expert FFN (T <= kGemvMaxTokens): gate/up GEMV + SwiGLU into h, then down GEMV with
-// the weighted combine into out.
-void launch_gateup_gemv(const WorkItem *work, const DevCounters *ctr, int max_work,
-                        const uint16_t *x, const int32_t *tok, uint16_t *h, int T, int d,
-                        int d_ff, cudaStream_t s);
-void launch_down_gemv(const WorkItem *work, const DevCounters *ctr, int max_work,
-                      const uint16_t *h, const int32_t *tok, const float *wq, uint16_t *out,
-                      int T, int d, int d_ff, cudaStream_t s);
+// Decode expert FFN (T <= kGemvMaxTokens): gate/up GEMV + SwiGLU into h; down GEMV into the
+// fp32 per-row buffer y [(T*k + T)][d]; then the weighted combine into out.
+void launch_gateup_gemv(const WorkItem *work, DevCounters *ctr, int max_work, const uint16_t *x,
+                        const int32_t *tok, uint16_t *h, int T, int d, int d_ff, cudaStream_t s);
+void launch_down_gemv(const WorkItem *work, DevCounters *ctr, int max_work, const uint16_t *h,
+                      const int32_t *inv, const float *w, float *y, uint16_t *out, int T, int k,
+                      int d, int d_ff, int shared, cudaStream_t s);
 
 // Grouped-GEMM expert FFN for larger T.
 void launch_gather_rows(const uint16_t *x, const int32_t *tok, uint16_t *xp, int rows, int d,
                         cudaStream_t s);
-void launch_gemm_gateup(const WorkItem *work, const DevCounters *ctr, int max_work, int max_rows,
-                        const uint16_t *xp, uint16_t *h, int d, int d_ff, cudaStream_t s);
-void launch_gemm_down(const WorkItem *work, const DevCounters *ctr, int max_work, int max_rows,
-                      const uint16_t *h, const int32_t *tok, const float *wq, float *acc, int d,
-                      int d_ff, cudaStream_t s);
 void launch_cast_out(const float *acc, uint16_t *out, size_t n, const DevCounters *ctr,
                      cudaStream_t s);
+
+// Tensor maps of the tcgen05 grouped GEMMs for one weight buffer (slots, a prefill buffer):
+// A views of the gathered activations and of h, B views of the buffer's entries (rows of d
+// for W_gate/W_up, rows of d_ff for W_down) and of the shared-expert array.
+struct TcMaps {
+  CUtensorMap a_x, a_h, b_gu, b_dn256, b_dn128, bs_gu, bs_dn256, bs_dn128;
+};
+// 2-D bf16 view [rows][inner] of base with a box of [box_rows][64] and 128-byte swizzle.
+bool make_tmap(CUtensorMap *m, const void *base, uint64_t inner, uint64_t rows, uint32_t box_rows);
+// gate/up then down (+ weighted red-add combine into acc) on the tensor cores.
+void launch_tc_ffn(const TcMaps &maps, const WorkItem *work, DevCounters *ctr, int *prefix,
+                   uint16_t *h, const int32_t *tok, const float *wq, float *acc, int d, int d_ff,
+                   int shared_entry, cudaStream_t s);
 
 // Record `code` and a message (with the CUDA error string if e != cudaSuccess) as this
 // thread's ft_last_error(); returns code.

@@ -11,6 +11,8 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <type_traits>
+
 #include "internal.h"
 
 namespace ftm {
@@ -103,17 +105,16 @@ __device__ __forceinline__ bool better(float va, int ia, float vb, int ib) {
   return va > vb || (va == vb && ia < ib);
 }
 
-__global__ void __launch_bounds__(256) k_topk(const float *__restrict__ logits, int32_t *idx,
-                                              float *w, uint8_t *tie, int T, int E, int k) {
+// One warp: top-k of one token's E logits (NV = ceil(E/32) values per lane).
+template <int NV>
+__device__ __forceinline__ void topk_warp(const float *__restrict__ row, int E, int k,
+                                          int32_t *idx_row, float *w_row, uint8_t *tie_t) {
   const int lane = threadIdx.x & 31;
-  const int t = (int)(((long)blockIdx.x * blockDim.x + threadIdx.x) >> 5);
-  if (t >= T) return;
-  float v[kMaxE / 32];
-  const int nv = (E + 31) >> 5;
+  float v[NV];
 #pragma unroll
-  for (int i = 0; i < kMaxE / 32; ++i) {
+  for (int i = 0; i < NV; ++i) {
     const int e = lane + 32 * i;
-    v[i] = (i < nv && e < E) ? logits[(size_t)t * E + e] : -INFINITY;
+    v[i] = (e < E) ? __ldcg(row + e) : -INFINITY;
   }
   uint32_t taken = 0;  // bit i: expert lane+32i already selected
   float sel_v = 0.f;   // lane j keeps the j-th selected logit
@@ -124,9 +125,9 @@ __global__ void __launch_bounds__(256) k_topk(const float *__restrict__ logits, 
     float bv = -INFINITY;
     int bi = 0x7fffffff;
 #pragma unroll
-    for (int i = 0; i < kMaxE / 32; ++i) {
+    for (int i = 0; i < NV; ++i) {
       const int e = lane + 32 * i;
-      if (i < nv && e < E && !((taken >> i) & 1u) && better(v[i], e, bv, bi)) {
+      if (e < E && !((taken >> i) & 1u) && better(v[i], e, bv, bi)) {
         bv = v[i];
         bi = e;
       }
@@ -163,16 +164,37 @@ __global__ void __launch_bounds__(256) k_topk(const float *__restrict__ logits, 
   if (lane == k - 1 && k < E) near = near || ((double)sel_v - (double)next_v) <= kNearTie;
   const bool any_near = __any_sync(0xffffffffu, near);
   if (lane < k) {
-    idx[(size_t)t * k + lane] = sel_i;
-    w[(size_t)t * k + lane] = ex / sum;
+    idx_row[lane] = sel_i;
+    w_row[lane] = ex / sum;
   }
-  if (lane == 0) tie[t] = any_near ? 1 : 0;
+  if (lane == 0) *tie_t = any_near ? 1 : 0;
+}
+
+template <int NV>
+__global__ void __launch_bounds__(256) k_topk(const float *__restrict__ logits, int32_t *idx,
+                                              float *w, uint8_t *tie, int T, int E, int k) {
+  const int t = (int)(((long)blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+  if (t >= T) return;
+  topk_warp<NV>(logits + (size_t)t * E, E, k, idx + (size_t)t * k, w + (size_t)t * k, tie + t);
+}
+
+template <typename F>
+void dispatch_nv(int E, F &&f) {
+  if (E <= 32) f(std::integral_constant<int, 1>{});
+  else if (E <= 64) f(std::integral_constant<int, 2>{});
+  else if (E <= 128) f(std::integral_constant<int, 4>{});
+  else if (E <= 256) f(std::integral_constant<int, 8>{});
+  else if (E <= 512) f(std::integral_constant<int, 16>{});
+  else f(std::integral_constant<int, 32>{});
 }
 
 void launch_topk(const float *logits, int32_t *idx, float *w, uint8_t *tie, int T, int E, int k,
                  cudaStream_t s) {
   const int threads = 256;
-  k_topk<<<(T * 32 + threads - 1) / threads, threads, 0, s>>>(logits, idx, w, tie, T, E, k);
+  const unsigned blocks = (unsigned)((T * 32 + threads - 1) / threads);
+  dispatch_nv(E, [&](auto nv) {
+    k_topk<decltype(nv)::value><<<blocks, threads, 0, s>>>(logits, idx, w, tie, T, E, k);
+  });
 }
 
 // ---------------------------------------------------------------------------------------
@@ -315,7 +337,7 @@ void launch_perm_multi(const ControlArgs &a, int32_t *chunk_scratch, cudaStream_
 // ---------------------------------------------------------------------------------------
 constexpr int kStampSmem = 2048;  // slots whose eviction keys are staged in shared memory
 
-__global__ void __launch_bounds__(1024) k_control(ControlArgs a, int perm_ready) {
+__device__ __forceinline__ void control_body(const ControlArgs &a, int perm_ready) {
   __shared__ int s_cnt[kMaxE];
   __shared__ int s_off[kMaxE + 1];
   __shared__ int s_base[kMaxE];
@@ -518,6 +540,106 @@ __global__ void __launch_bounds__(1024) k_control(ControlArgs a, int perm_ready)
     }
     a.ctr->n_work = nw;
   }
+}
+
+__global__ void __launch_bounds__(1024) k_control(ControlArgs a, int perm_ready) {
+  control_body(a, perm_ready);
+}
+
+// ---------------------------------------------------------------------------------------
+// Decode routing in one launch (T <= kGemvMaxTokens): every CTA computes a block of router
+// logits; the CTA that finishes last (atomic arrival counter, no waiting) runs the top-k of
+// all T tokens, one warp per token, and then the control body above.
+// ---------------------------------------------------------------------------------------
+template <int TT, int EE, int NV>
+__global__ void __launch_bounds__(1024) k_route_decode(const uint16_t *__restrict__ x,
+                                                       const uint16_t *__restrict__ wr,
+                                                       const float *__restrict__ bias,
+                                                       float *__restrict__ logits,
+                                                       ControlArgs a) {
+  const int T = a.T, E = a.E;
+  const int lane = threadIdx.x & 31;
+  const int n_eb = (E + EE - 1) / EE;
+  const int n_tasks = ((T + TT - 1) / TT) * n_eb;
+  const int task = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+  if (task < n_tasks) {
+    const int tb = task / n_eb, eb = task - tb * n_eb;
+    const int t0 = tb * TT, e0 = eb * EE;
+    float acc[TT][EE];
+#pragma unroll
+    for (int i = 0; i < TT; ++i)
+#pragma unroll
+      for (int j = 0; j < EE; ++j) acc[i][j] = 0.f;
+    const int d = a.d, nchunk = d >> 3;
+#pragma unroll 2
+    for (int c = lane; c < nchunk; c += 32) {
+      uint4 xv[TT], wv[EE];
+#pragma unroll
+      for (int i = 0; i < TT; ++i)
+        xv[i] = (t0 + i < T) ? __ldg(reinterpret_cast<const uint4 *>(x + (size_t)(t0 + i) * d) + c)
+                             : make_uint4(0, 0, 0, 0);
+#pragma unroll
+      for (int j = 0; j < EE; ++j)
+        wv[j] = (e0 + j < E) ? __ldg(reinterpret_cast<const uint4 *>(wr + (size_t)(e0 + j) * d) + c)
+                             : make_uint4(0, 0, 0, 0);
+#pragma unroll
+      for (int i = 0; i < TT; ++i)
+#pragma unroll
+        for (int j = 0; j < EE; ++j) acc[i][j] = dot8_seq(xv[i], wv[j], acc[i][j]);
+    }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1)
+#pragma unroll
+      for (int i = 0; i < TT; ++i)
+#pragma unroll
+        for (int j = 0; j < EE; ++j)
+          acc[i][j] = acc[i][j] + __shfl_xor_sync(0xffffffffu, acc[i][j], off);
+#pragma unroll
+    for (int i = 0; i < TT; ++i)
+#pragma unroll
+      for (int j = 0; j < EE; ++j) {
+        if (lane == ((i * EE + j) & 31) && t0 + i < T && e0 + j < E) {
+          float v = acc[i][j];
+          if (bias) v = v + bias[e0 + j];
+          logits[(size_t)(t0 + i) * E + e0 + j] = v;
+        }
+      }
+  }
+  // the last CTA to arrive continues
+  __shared__ int s_last;
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const unsigned prev = atomicAdd(&a.ctr->route_arrive, 1u);
+    s_last = (prev == gridDim.x - 1) ? 1 : 0;
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  const int warp = threadIdx.x >> 5;
+  for (int t = warp; t < T; t += 32)
+    topk_warp<NV>(logits + (size_t)t * E, E, a.k, const_cast<int32_t *>(a.idx) + (size_t)t * a.k,
+                  const_cast<float *>(a.w) + (size_t)t * a.k, const_cast<uint8_t *>(a.tie) + t);
+  __syncthreads();
+  if (threadIdx.x == 0) a.ctr->route_arrive = 0;
+  control_body(a, 0);
+}
+
+void launch_route_decode(const uint16_t *x, const uint16_t *wr, const float *bias, float *logits,
+                         const ControlArgs &a, cudaStream_t s) {
+  dispatch_nv(a.E, [&](auto nv) {
+    constexpr int NV = decltype(nv)::value;
+    auto go = [&](auto kern, int tt, int ee) {
+      const int tasks = ((a.T + tt - 1) / tt) * ((a.E + ee - 1) / ee);
+      kern<<<(tasks + 31) / 32, 1024, 0, s>>>(x, wr, bias, logits, a);
+    };
+    if (a.T == 1)
+      go(k_route_decode<1, 1, NV>, 1, 1);
+    else if (a.T <= 2)
+      go(k_route_decode<2, 2, NV>, 2, 2);
+    else
+      go(k_route_decode<4, 2, NV>, 4, 2);
+  });
 }
 
 void launch_control(const ControlArgs &a, bool perm_ready, cudaStream_t s) {

@@ -205,11 +205,13 @@ int ft_moe_get_dims(ft_moe *h, int32_t dims[8]);
 
 /*
  * Kernel timing for roofline measurement.  While enabled, forward and prefill bracket every
- * kernel launch with a pair of CUDA events on the launching stream (so the enabled calls
- * must not be captured).  ft_moe_profile_read synchronises, adds the elapsed time and
- * launch count of each kernel class to ms[] / launches[] (arrays of FT_PROF_N, zeroed by the
- * caller) and clears the record.  Recording adds a few microseconds per launch; time the
- * throughput with profiling off.
+ * kernel launch with a pair of CUDA events on the launching stream.  enable = 1: eager calls;
+ * ft_moe_profile_read synchronises, adds the elapsed time and launch count of each kernel
+ * class to ms[] / launches[] (arrays of FT_PROF_N, zeroed by the caller) and clears the
+ * record.  enable = 2: graph mode; the events (for up to 4096 launches) are created now, the
+ * calls are then captured into a CUDA graph (their event records become graph nodes), and
+ * ft_moe_profile_read after each replay adds that replay's times, keeping the record.
+ * enable = 0 stops.  Recording adds a little time per launch; time throughput with it off.
  */
 enum {
   FT_PROF_ROUTER = 0,   /* router logits                                   */
