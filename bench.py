@@ -569,6 +569,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batches", default="", help="comma list of decode batch sizes")
     ap.add_argument("--slots", type=int, default=0, help="override the slot count")
+    ap.add_argument("--experts", type=int, default=0, help="override E (profiling cases)")
+    ap.add_argument("--layers", type=int, default=0, help="override L (profiling cases)")
+    ap.add_argument("--tokens", default="", help="prefill token counts, comma list")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -579,6 +582,12 @@ def main():
             wl["headline_b"] = wl["batches"][0]
     if args.slots:
         wl["n_slots"] = args.slots
+    if args.experts:
+        wl["E"] = args.experts
+    if args.layers:
+        wl["L"] = args.layers
+    if args.tokens:
+        wl["tokens"] = tuple(int(v) for v in args.tokens.split(","))
     import torch
     if args.impl == "reference":
         rank = int(os.environ.get("RANK", "0"))

@@ -8,6 +8,25 @@
 
 namespace ftm {
 
+// Launch `kern` on `s` with programmatic stream serialization, so it may begin while the
+// previous kernel on the stream finishes; the kernel calls pdl_wait() before reading that
+// kernel's results.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t s, Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
 constexpr int kMaxE = 1024;        // experts per layer
 constexpr int kMaxK = 32;          // routed experts per token
 constexpr int kGemvMaxTokens = 16; // forward calls with T <= this use the GEMV kernels
@@ -74,6 +93,12 @@ __device__ __forceinline__ uint16_t f32_to_bf16(float f) {
   u += 0x7FFFu + ((u >> 16) & 1u);
   return (uint16_t)(u >> 16);
 }
+
+// Programmatic dependent launch: let the next kernel on the stream start launching now, and
+// wait here until the previous kernel has completed and its writes are visible.  Both are
+// no-ops for kernels launched without the programmatic-serialization attribute.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 __device__ __forceinline__ void set_status(DevCounters *c, int code) {
   atomicCAS(&c->status, 0, code);

@@ -24,13 +24,18 @@ __device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f +
 
 // ---------------------------------------------------------------------------------------
 // Miss fill: every fill-list entry (slot, layer, expert) is copied from the mapped pinned
-// host pool to its slot by SM loads over the host link.  The grid is fixed; the count is
-// read on the device, so the launch needs no host round trip and can be captured.
+// host pool to its slot by SM loads over the host link (16 bytes per thread per load, kFillU
+// loads in flight per thread).  The grid is fixed; the count is read on the device, so the
+// launch needs no host round trip and can be captured.
 // ---------------------------------------------------------------------------------------
+constexpr int kFillU = 8;
+
 __global__ void __launch_bounds__(512) k_fill(const uint4 *__restrict__ pool, uint4 *slots,
                                               const int32_t *__restrict__ fills,
                                               const DevCounters *__restrict__ ctr,
                                               size_t entry_vec, int E) {
+  pdl_trigger();
+  pdl_wait();
   const int n = ctr->n_fill;
   const size_t stride = (size_t)gridDim.x * blockDim.x;
   const size_t t0 = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -39,25 +44,22 @@ __global__ void __launch_bounds__(512) k_fill(const uint4 *__restrict__ pool, ui
     const uint4 *src = pool + ((size_t)l * E + e) * entry_vec;
     uint4 *dst = slots + (size_t)slot * entry_vec;
     size_t i = t0;
-    for (; i + 3 * stride < entry_vec; i += 4 * stride) {
-      const uint4 a = src[i], b = src[i + stride], c = src[i + 2 * stride],
-                  d = src[i + 3 * stride];
-      dst[i] = a;
-      dst[i + stride] = b;
-      dst[i + 2 * stride] = c;
-      dst[i + 3 * stride] = d;
+    for (; i + (kFillU - 1) * stride < entry_vec; i += kFillU * stride) {
+      uint4 v[kFillU];
+#pragma unroll
+      for (int u = 0; u < kFillU; ++u) v[u] = src[i + u * stride];
+#pragma unroll
+      for (int u = 0; u < kFillU; ++u) dst[i + u * stride] = v[u];
     }
     for (; i < entry_vec; i += stride) dst[i] = src[i];
   }
 }
 
 void launch_fill(const uint16_t *pool_dev, uint16_t *slots, const int32_t *fills,
-                 const DevCounters *ctr, size_t entry_bytes, int E, int max_fill,
-                 cudaStream_t s) {
+                 DevCounters *ctr, size_t entry_bytes, int E, int max_fill, cudaStream_t s) {
   (void)max_fill;
-  k_fill<<<148 * 2, 512, 0, s>>>(reinterpret_cast<const uint4 *>(pool_dev),
-                                 reinterpret_cast<uint4 *>(slots), fills, ctr, entry_bytes / 16,
-                                 E);
+  launch_pdl(k_fill, dim3(148), dim3(512), 0, s, reinterpret_cast<const uint4 *>(pool_dev),
+             reinterpret_cast<uint4 *>(slots), fills, (const DevCounters *)ctr, entry_bytes / 16, E);
 }
 
 // ---------------------------------------------------------------------------------------
@@ -167,8 +169,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) k_gateup_tma(
     const uint16_t *__restrict__ x, const int32_t *__restrict__ tok, uint16_t *__restrict__ h,
     int T, int d, int d_ff, int R, uint32_t stage_bytes) {
   extern __shared__ __align__(128) uint8_t smem[];
-  if (ctr->call_status != 0) return;
-  const int n_work = ctr->n_work;
+  pdl_trigger();
   const int nchunk = d >> 3;
   const size_t x_bytes = XS ? (size_t)T * d * 2 : 0;
   RingSmem r = ring_layout(smem, x_bytes, stage_bytes);
@@ -178,6 +179,9 @@ __global__ void __launch_bounds__(kGemvThreads, 1) k_gateup_tma(
       reinterpret_cast<uint4 *>(smem)[i] = __ldg(reinterpret_cast<const uint4 *>(x) + i);
   ring_init(r);
   __syncthreads();
+  pdl_wait();  // the work list, the fills and the slot table come from the kernels before
+  if (ctr->call_status != 0) return;
+  const int n_work = ctr->n_work;
   const int n_jb = (d_ff + R - 1) / R;
   const long n_tasks = (long)n_work * n_jb;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -244,12 +248,14 @@ __global__ void __launch_bounds__(kGemvThreads, 1) k_down_tma(
     const uint16_t *__restrict__ h, float *__restrict__ y, int d, int d_ff, int R,
     uint32_t stage_bytes) {
   extern __shared__ __align__(128) uint8_t smem[];
-  if (ctr->call_status != 0) return;
-  const int n_work = ctr->n_work;
+  pdl_trigger();
   const int nchunk = d_ff >> 3;
   RingSmem r = ring_layout(smem, 0, stage_bytes);
   ring_init(r);
   __syncthreads();
+  pdl_wait();  // h comes from the gate/up kernel
+  if (ctr->call_status != 0) return;
+  const int n_work = ctr->n_work;
   const int n_ib = (d + R - 1) / R;
   const long n_tasks = (long)n_work * n_ib;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -329,7 +335,8 @@ void launch_gateup_gemv(const WorkItem *work, DevCounters *ctr, int max_work, co
   const size_t smem = ring_smem_bytes(xs ? (size_t)T * d * 2 : 0, sb);
   auto go = [&](auto kern) {
     allow_smem(kern, smem);
-    kern<<<sm_count(), kGemvThreads, smem, s>>>(work, ctr, x, tok, h, T, d, d_ff, R, sb);
+    launch_pdl(kern, dim3(sm_count()), dim3(kGemvThreads), smem, s, work, ctr, x, tok, h, T, d,
+               d_ff, R, sb);
   };
   if (T <= 1)
     xs ? go(k_gateup_tma<1, true>) : go(k_gateup_tma<1, false>);
@@ -344,6 +351,8 @@ void launch_gateup_gemv(const WorkItem *work, DevCounters *ctr, int max_work, co
 __global__ void k_combine(const float *__restrict__ y, const float *__restrict__ w,
                           const int32_t *__restrict__ inv, const DevCounters *__restrict__ ctr,
                           uint16_t *__restrict__ out, int T, int k, int d, int shared) {
+  pdl_trigger();
+  pdl_wait();
   if (ctr->call_status != 0) return;
   const int n8 = d >> 3;
   const int gidx = blockIdx.x * blockDim.x + threadIdx.x;
@@ -394,7 +403,8 @@ void launch_down_gemv(const WorkItem *work, DevCounters *ctr, int max_work, cons
   const size_t smem = ring_smem_bytes(0, sb);
   auto go = [&](auto kern) {
     allow_smem(kern, smem);
-    kern<<<sm_count(), kGemvThreads, smem, s>>>(work, ctr, h, y, d, d_ff, R, sb);
+    launch_pdl(kern, dim3(sm_count()), dim3(kGemvThreads), smem, s, work, ctr, h, y, d, d_ff, R,
+               sb);
   };
   if (T <= 1)
     go(k_down_tma<1>);
@@ -403,7 +413,8 @@ void launch_down_gemv(const WorkItem *work, DevCounters *ctr, int max_work, cons
   else
     go(k_down_tma<16>);
   const int n = T * (d >> 3);
-  k_combine<<<(n + 255) / 256, 256, 0, s>>>(y, w, inv, ctr, out, T, k, d, shared);
+  launch_pdl(k_combine, dim3((n + 255) / 256), dim3(256), 0, s, (const float *)y, w, inv,
+             (const DevCounters *)ctr, out, T, k, d, shared);
 }
 
 // ---------------------------------------------------------------------------------------

@@ -168,3 +168,4 @@ __device__ __forceinline__ void red_add_v4(float *addr, float a, float b, float 
 }
 
 }  // namespace ftm
+

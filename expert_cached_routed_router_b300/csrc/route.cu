@@ -557,6 +557,7 @@ __global__ void __launch_bounds__(1024) k_route_decode(const uint16_t *__restric
                                                        const float *__restrict__ bias,
                                                        float *__restrict__ logits,
                                                        ControlArgs a) {
+  pdl_trigger();
   const int T = a.T, E = a.E;
   const int lane = threadIdx.x & 31;
   const int n_eb = (E + EE - 1) / EE;
@@ -605,6 +606,8 @@ __global__ void __launch_bounds__(1024) k_route_decode(const uint16_t *__restric
         }
       }
   }
+  // the previous kernel (which reads the routing state this launch rewrites) must be done
+  pdl_wait();
   // the last CTA to arrive continues
   __shared__ int s_last;
   __threadfence();
@@ -631,7 +634,7 @@ void launch_route_decode(const uint16_t *x, const uint16_t *wr, const float *bia
     constexpr int NV = decltype(nv)::value;
     auto go = [&](auto kern, int tt, int ee) {
       const int tasks = ((a.T + tt - 1) / tt) * ((a.E + ee - 1) / ee);
-      kern<<<(tasks + 31) / 32, 1024, 0, s>>>(x, wr, bias, logits, a);
+      launch_pdl(kern, dim3((tasks + 31) / 32), dim3(1024), 0, s, x, wr, bias, logits, a);
     };
     if (a.T == 1)
       go(k_route_decode<1, 1, NV>, 1, 1);
