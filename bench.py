@@ -403,11 +403,14 @@ def run_decode(args, wl, rank, world):
                          f"({calls / wl['L']:.2f} decode steps), {el:.1f} s, numpy fp32 router "
                          f"+ fp64 experts, single thread"}
     g = rl["gateup"]
-    roof = {"bound": "hbm", "kernel": "k_gateup_gemv (gate/up + SwiGLU, decode)",
+    # DRAM bytes per launch of k_gateup_tma at b = 1 (8 touched experts) from the committed ncu
+    # capture (profiles/decode_kernels_full_capture.md); only valid for that shape
+    traffic = 50.47e6 if (args.workload == "decode24" and b == 1) else None
+    roof = {"bound": "hbm", "kernel": "k_gateup_tma (gate/up + SwiGLU, decode)",
             "achieved": round(g["achieved"], 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
-            "frac": round(g["achieved"] / pk["hbm_gbs"], 4), "traffic": None,
+            "frac": round(g["achieved"] / pk["hbm_gbs"], 4), "traffic": traffic,
             "peak_source": pk["source"],
-            "algorithmic_bytes": "touched experts x 2*d_ff*d*2 B per call"}
+            "algorithmic_bytes": "touched experts x 2*d_ff*d*2 B per call (50.33 MB at b=1)"}
     line = {
         "metric": "MoE-layer tokens/s (decode trace, b=1)",
         "value": round(res["tok_s_all"], 2), "unit": "tokens/s", "n_gpus": world,
