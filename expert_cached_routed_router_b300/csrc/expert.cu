@@ -96,18 +96,19 @@ struct RingSmem {
 };
 
 // Carve the dynamic shared memory: [x staging | stages | barriers].
-__device__ __forceinline__ RingSmem ring_layout(uint8_t *smem, size_t x_bytes, uint32_t stage_bytes) {
+__device__ __forceinline__ RingSmem ring_layout(uint8_t *smem, size_t x_bytes, uint32_t stage_bytes,
+                                                uint32_t ring_bytes) {
   RingSmem r;
   r.base = smem + ((x_bytes + 127) & ~(size_t)127);
   r.stage_bytes = stage_bytes;
-  r.n = (int)min((uint32_t)kMaxStages, kRingBytes / stage_bytes);
+  r.n = (int)min((uint32_t)kMaxStages, ring_bytes / stage_bytes);
   r.full = reinterpret_cast<uint64_t *>(r.base + (size_t)r.n * stage_bytes);
   r.empty = r.full + r.n;
   return r;
 }
 
-static size_t ring_smem_bytes(size_t x_bytes, uint32_t stage_bytes) {
-  const int n = (int)std::min((uint32_t)kMaxStages, kRingBytes / stage_bytes);
+static size_t ring_smem_bytes(size_t x_bytes, uint32_t stage_bytes, uint32_t ring_bytes) {
+  const int n = (int)std::min((uint32_t)kMaxStages, ring_bytes / stage_bytes);
   return ((x_bytes + 127) & ~(size_t)127) + (size_t)n * stage_bytes + 2 * n * 8;
 }
 
@@ -161,18 +162,53 @@ __device__ __forceinline__ bool ring_consume(RingSmem &r, long n_tasks, Use use)
   return true;
 }
 
+// Token groups: an item's c tokens are processed G at a time (G = 1 or 4); the weight rows
+// sit in shared memory, so going over them once per group costs shared-memory bandwidth only.
+template <int G, bool XS>
+__device__ __forceinline__ void gateup_rows(const uint4 *__restrict__ g, const uint4 *__restrict__ uu,
+                                            const uint4 *__restrict__ xs, const int32_t *tk,
+                                            int n, int nchunk, int lane, float (&ag)[G],
+                                            float (&au)[G]) {
+  int row[G];
+#pragma unroll
+  for (int t = 0; t < G; ++t) {
+    ag[t] = au[t] = 0.f;
+    row[t] = (t < n) ? tk[t] * nchunk : 0;
+  }
+  for (int ch = lane; ch < nchunk; ch += 32) {
+    const uint4 gv = g[ch], uv = uu[ch];
+#pragma unroll
+    for (int t = 0; t < G; ++t) {
+      if (t < n) {
+        const uint4 xv = XS ? xs[row[t] + ch] : __ldg(xs + row[t] + ch);
+        ag[t] = dot8_seq(gv, xv, ag[t]);
+        au[t] = dot8_seq(uv, xv, au[t]);
+      }
+    }
+  }
+#pragma unroll
+  for (int t = 0; t < G; ++t) {
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) {
+      ag[t] += __shfl_xor_sync(0xffffffffu, ag[t], off);
+      au[t] += __shfl_xor_sync(0xffffffffu, au[t], off);
+    }
+  }
+}
+
 // gate/up + SwiGLU.  Task = (item u, rows j0 .. j0+R-1 of W_gate and of W_up); stage =
-// [R gate rows | R up rows].  h[q][j] = silu(g) * u (bf16).
-template <int MAXT, bool XS>
+// [R gate rows | R up rows].  h[q][j] = silu(g) * u (bf16).  x is staged in shared memory
+// when it fits next to the ring (XS).
+template <bool XS>
 __global__ void __launch_bounds__(kGemvThreads, 1) k_gateup_tma(
     const WorkItem *__restrict__ work, DevCounters *__restrict__ ctr,
     const uint16_t *__restrict__ x, const int32_t *__restrict__ tok, uint16_t *__restrict__ h,
-    int T, int d, int d_ff, int R, uint32_t stage_bytes) {
+    int T, int d, int d_ff, int R, uint32_t stage_bytes, uint32_t ring_bytes) {
   extern __shared__ __align__(128) uint8_t smem[];
   pdl_trigger();
   const int nchunk = d >> 3;
   const size_t x_bytes = XS ? (size_t)T * d * 2 : 0;
-  RingSmem r = ring_layout(smem, x_bytes, stage_bytes);
+  RingSmem r = ring_layout(smem, x_bytes, stage_bytes, ring_bytes);
   const uint4 *xs = XS ? reinterpret_cast<const uint4 *>(smem) : reinterpret_cast<const uint4 *>(x);
   if (XS)
     for (int i = threadIdx.x; i < T * nchunk; i += blockDim.x)
@@ -202,37 +238,24 @@ __global__ void __launch_bounds__(kGemvThreads, 1) k_gateup_tma(
       const int u = (int)(task / n_jb), j0 = (int)(task - (long)u * n_jb) * R;
       const int rows = min(R, d_ff - j0);
       const WorkItem wi = work[u];
-      const int c = min(wi.count, MAXT);
-      int tk[MAXT];
-#pragma unroll
-      for (int t = 0; t < MAXT; ++t) tk[t] = (t < c) ? tok[wi.q0 + t] : 0;
+      const int c = wi.count;
       for (int rr = 0; rr < rows; ++rr) {
         const uint4 *g = reinterpret_cast<const uint4 *>(st + (size_t)rr * d * 2);
         const uint4 *uu = reinterpret_cast<const uint4 *>(st + (size_t)(R + rr) * d * 2);
-        float ag[MAXT], au[MAXT];
+        for (int t0 = 0; t0 < c; t0 += 4) {
+          const int n = min(4, c - t0);
+          const int32_t *tk = tok + wi.q0 + t0;
+          uint16_t *hq = h + (size_t)(wi.q0 + t0) * d_ff + j0 + rr;
+          if (n == 1) {
+            float ag[1], au[1];
+            gateup_rows<1, XS>(g, uu, xs, tk, 1, nchunk, lane, ag, au);
+            if (lane == 0) hq[0] = f32_to_bf16(silu_mul(ag[0], au[0]));
+          } else {
+            float ag[4], au[4];
+            gateup_rows<4, XS>(g, uu, xs, tk, n, nchunk, lane, ag, au);
 #pragma unroll
-        for (int t = 0; t < MAXT; ++t) ag[t] = au[t] = 0.f;
-        for (int ch = lane; ch < nchunk; ch += 32) {
-          const uint4 gv = g[ch], uv = uu[ch];
-#pragma unroll
-          for (int t = 0; t < MAXT; ++t) {
-            if (t < c) {
-              const uint4 xv = XS ? xs[tk[t] * nchunk + ch] : __ldg(xs + (size_t)tk[t] * nchunk + ch);
-              ag[t] = dot8_seq(gv, xv, ag[t]);
-              au[t] = dot8_seq(uv, xv, au[t]);
-            }
-          }
-        }
-#pragma unroll
-        for (int t = 0; t < MAXT; ++t) {
-          if (t < c) {
-#pragma unroll
-            for (int off = 16; off >= 1; off >>= 1) {
-              ag[t] += __shfl_xor_sync(0xffffffffu, ag[t], off);
-              au[t] += __shfl_xor_sync(0xffffffffu, au[t], off);
-            }
-            if (lane == t)
-              h[(size_t)(wi.q0 + t) * d_ff + j0 + rr] = f32_to_bf16(silu_mul(ag[t], au[t]));
+            for (int t = 0; t < 4; ++t)
+              if (lane == t && t < n) hq[(size_t)t * d_ff] = f32_to_bf16(silu_mul(ag[t], au[t]));
           }
         }
       }
@@ -241,16 +264,51 @@ __global__ void __launch_bounds__(kGemvThreads, 1) k_gateup_tma(
   if (!ok) set_status(ctr, FT_ERR_TIMEOUT);
 }
 
+// Up to kDownRows W_down rows of a task against G token rows of h: every h chunk is loaded once
+// and used for all the task's rows (held in shared memory).
+constexpr int kDownRows = 8;
+
+template <int G>
+__device__ __forceinline__ void down_rows(const uint8_t *__restrict__ st, int rows,
+                                          const uint16_t *__restrict__ hq, int n, int d_ff,
+                                          int nchunk, int lane, float (&part)[kDownRows][G]) {
+#pragma unroll
+  for (int r = 0; r < kDownRows; ++r)
+#pragma unroll
+    for (int t = 0; t < G; ++t) part[r][t] = 0.f;
+  for (int ch = lane; ch < nchunk; ch += 32) {
+    uint4 hv[G];
+#pragma unroll
+    for (int t = 0; t < G; ++t)
+      hv[t] = (t < n) ? __ldg(reinterpret_cast<const uint4 *>(hq + (size_t)t * d_ff) + ch)
+                      : make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int r = 0; r < kDownRows; ++r) {
+      if (r < rows) {
+        const uint4 wv = reinterpret_cast<const uint4 *>(st + (size_t)r * d_ff * 2)[ch];
+#pragma unroll
+        for (int t = 0; t < G; ++t) part[r][t] = dot8_seq(wv, hv[t], part[r][t]);
+      }
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < kDownRows; ++r)
+#pragma unroll
+    for (int t = 0; t < G; ++t)
+#pragma unroll
+      for (int off = 16; off >= 1; off >>= 1)
+        part[r][t] += __shfl_xor_sync(0xffffffffu, part[r][t], off);
+}
+
 // down: task = (item u, rows i0 .. i0+R-1 of W_down); y[q][i] fp32 for the item's rows q.
-template <int MAXT>
 __global__ void __launch_bounds__(kGemvThreads, 1) k_down_tma(
     const WorkItem *__restrict__ work, DevCounters *__restrict__ ctr,
     const uint16_t *__restrict__ h, float *__restrict__ y, int d, int d_ff, int R,
-    uint32_t stage_bytes) {
+    uint32_t stage_bytes, uint32_t ring_bytes) {
   extern __shared__ __align__(128) uint8_t smem[];
   pdl_trigger();
   const int nchunk = d_ff >> 3;
-  RingSmem r = ring_layout(smem, 0, stage_bytes);
+  RingSmem r = ring_layout(smem, 0, stage_bytes, ring_bytes);
   ring_init(r);
   __syncthreads();
   pdl_wait();  // h comes from the gate/up kernel
@@ -274,28 +332,25 @@ __global__ void __launch_bounds__(kGemvThreads, 1) k_down_tma(
       const int u = (int)(task / n_ib), i0 = (int)(task - (long)u * n_ib) * R;
       const int rows = min(R, d - i0);
       const WorkItem wi = work[u];
-      const int c = min(wi.count, MAXT);
-      for (int rr = 0; rr < rows; ++rr) {
-        const uint4 *wrow = reinterpret_cast<const uint4 *>(st + (size_t)rr * d_ff * 2);
-        float part[MAXT];
+      const int c = wi.count;
+      for (int t0 = 0; t0 < c; t0 += 4) {
+        const int n = min(4, c - t0);
+        const uint16_t *hq = h + (size_t)(wi.q0 + t0) * d_ff;
+        float *yq = y + (size_t)(wi.q0 + t0) * d + i0;
+        if (n == 1) {
+          float part[kDownRows][1];
+          down_rows<1>(st, rows, hq, 1, d_ff, nchunk, lane, part);
 #pragma unroll
-        for (int t = 0; t < MAXT; ++t) part[t] = 0.f;
-        for (int ch = lane; ch < nchunk; ch += 32) {
-          const uint4 wv = wrow[ch];
+          for (int r = 0; r < kDownRows; ++r)
+            if (lane == r && r < rows) yq[r] = part[r][0];
+        } else {
+          float part[kDownRows][4];
+          down_rows<4>(st, rows, hq, n, d_ff, nchunk, lane, part);
 #pragma unroll
-          for (int t = 0; t < MAXT; ++t)
-            if (t < c)
-              part[t] = dot8_seq(
-                  wv, __ldg(reinterpret_cast<const uint4 *>(h + (size_t)(wi.q0 + t) * d_ff) + ch),
-                  part[t]);
-        }
+          for (int r = 0; r < kDownRows; ++r)
 #pragma unroll
-        for (int t = 0; t < MAXT; ++t) {
-          if (t < c) {
-#pragma unroll
-            for (int off = 16; off >= 1; off >>= 1) part[t] += __shfl_xor_sync(0xffffffffu, part[t], off);
-            if (lane == t) y[(size_t)(wi.q0 + t) * d + i0 + rr] = part[t];
-          }
+            for (int t = 0; t < 4; ++t)
+              if (lane == r * 4 + t && r < rows && t < n) yq[(size_t)t * d + r] = part[r][t];
         }
       }
     });
@@ -331,19 +386,21 @@ void launch_gateup_gemv(const WorkItem *work, DevCounters *ctr, int max_work, co
   (void)max_work;
   const uint32_t sb = stage_bytes_for(4u * d);
   const int R = std::max(1, std::min(d_ff, (int)(sb / (4u * d))));
-  const bool xs = (size_t)T * d * 2 <= (32u << 10);
-  const size_t smem = ring_smem_bytes(xs ? (size_t)T * d * 2 : 0, sb);
+  // x next to the ring when at least 4 stages still fit in 224 KB
+  const size_t xb = (size_t)T * d * 2;
+  const bool xs = xb + 4 * (size_t)sb <= (224u << 10);
+  const uint32_t ring = xs ? (uint32_t)std::min<size_t>(kRingBytes, (224u << 10) - ((xb + 127) & ~(size_t)127))
+                           : kRingBytes;
+  const size_t smem = ring_smem_bytes(xs ? xb : 0, sb, ring);
   auto go = [&](auto kern) {
     allow_smem(kern, smem);
     launch_pdl(kern, dim3(sm_count()), dim3(kGemvThreads), smem, s, work, ctr, x, tok, h, T, d,
-               d_ff, R, sb);
+               d_ff, R, sb, ring);
   };
-  if (T <= 1)
-    xs ? go(k_gateup_tma<1, true>) : go(k_gateup_tma<1, false>);
-  else if (T <= 4)
-    xs ? go(k_gateup_tma<4, true>) : go(k_gateup_tma<4, false>);
+  if (xs)
+    go(k_gateup_tma<true>);
   else
-    xs ? go(k_gateup_tma<16, true>) : go(k_gateup_tma<16, false>);
+    go(k_gateup_tma<false>);
 }
 
 // out[t][i] = sum_j w[t][j] * y[inv[t*k+j]][i] (j ascending) + y[P+t][i] for the shared
@@ -399,19 +456,11 @@ void launch_down_gemv(const WorkItem *work, DevCounters *ctr, int max_work, cons
                       int d, int d_ff, int shared, cudaStream_t s) {
   (void)max_work;
   const uint32_t sb = stage_bytes_for(2u * d_ff);
-  const int R = std::max(1, std::min(d, (int)(sb / (2u * d_ff))));
-  const size_t smem = ring_smem_bytes(0, sb);
-  auto go = [&](auto kern) {
-    allow_smem(kern, smem);
-    launch_pdl(kern, dim3(sm_count()), dim3(kGemvThreads), smem, s, work, ctr, h, y, d, d_ff, R,
-               sb);
-  };
-  if (T <= 1)
-    go(k_down_tma<1>);
-  else if (T <= 4)
-    go(k_down_tma<4>);
-  else
-    go(k_down_tma<16>);
+  const int R = std::max(1, std::min({d, kDownRows, (int)(sb / (2u * d_ff))}));
+  const size_t smem = ring_smem_bytes(0, sb, kRingBytes);
+  allow_smem(k_down_tma, smem);
+  launch_pdl(k_down_tma, dim3(sm_count()), dim3(kGemvThreads), smem, s, work, ctr, h, y, d, d_ff,
+             R, sb, kRingBytes);
   const int n = T * (d >> 3);
   launch_pdl(k_combine, dim3((n + 255) / 256), dim3(256), 0, s, (const float *)y, w, inv,
              (const DevCounters *)ctr, out, T, k, d, shared);

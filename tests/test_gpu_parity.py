@@ -196,3 +196,24 @@ def test_forward_is_deterministic():
     b = _run(st, 0, x).cpu().numpy()
     np.testing.assert_array_equal(a, b)
     st.close()
+
+
+def test_resize_allocation_failure_leaves_cache_intact(monkeypatch):
+    """An injected allocation failure during resize returns FT_ERR_OOM and changes nothing."""
+    import expert_cached_routed_router_b300 as ftm
+    cfg = Config(L=2, E=16, k=2, d=256, d_ff=128, n_slots=8, seed=9)
+    st = make_stack(cfg, max_tokens=16)
+    x = ft_synth.activations(9, 0, 3, cfg.d)
+    _run(st, 0, x)
+    before = st.cache_state()
+    monkeypatch.setenv("FT_FAULT_INJECT", "resize_alloc")
+    with pytest.raises(ftm.FtError) as ei:
+        st.resize(4)
+    assert ei.value.code == ftm.FT_ERR_OOM
+    monkeypatch.delenv("FT_FAULT_INJECT")
+    after = st.cache_state()
+    for a, b in zip(before, after):
+        np.testing.assert_array_equal(np.asarray(a), np.asarray(b))
+    st.resize(4)          # a real resize still works afterwards
+    assert st.stats()["n_slots"] == 4
+    st.close()
