@@ -132,7 +132,8 @@ def max_over_ranks(v, world):
         return v
     import torch
     import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
 
@@ -432,7 +433,10 @@ def run_decode(args, wl, rank, world):
         "cpu_baseline": cpu,
         "e2e": {"value": round(res["e2e_tok_s_all"], 2), "unit": "tokens/s",
                 "h2d_bytes_per_step": res["e2e"]["h2d"], "d2h_bytes_per_step": res["e2e"]["d2h"]},
-        "gpu_launches": int(sum(v[1] for v in prof.values()) / prof_k * args.steps),
+        # kernels per decode layer call: routing, fill, gate/up, down, combine (the "down"
+        # timing scope covers down + combine)
+        "gpu_launches": int((sum(v[1] for v in prof.values()) + prof["down"][1]) / prof_k
+                            * args.steps),
         "clocks": res["clocks"],
     }
     return line

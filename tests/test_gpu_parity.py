@@ -217,3 +217,61 @@ def test_resize_allocation_failure_leaves_cache_intact(monkeypatch):
     st.resize(4)          # a real resize still works afterwards
     assert st.stats()["n_slots"] == 4
     st.close()
+
+
+def test_decode_step_graph_capture_matches_eager():
+    """One decode step (several layers, shared cache) captured into a CUDA graph and replayed
+    gives the same outputs and the same cache state as the same calls run eagerly."""
+    import torch
+    cfg = Config(L=3, E=16, k=2, d=256, d_ff=128, n_slots=10, seed=10)
+    gen = ft_synth.DriftingZipfBias(10, cfg.L, cfg.E, s=0.8, sigma_walk=0.3)
+    steps = []
+    for t in range(6):
+        gen.advance()
+        steps.append((ft_synth.activations(10, t, 4, cfg.d),
+                      np.stack([gen.bias(l) for l in range(cfg.L)])))
+    pool = None
+
+    def run(use_graph):
+        nonlocal pool
+        st = make_stack(cfg, max_tokens=16, pool=pool)
+        pool = st._pool
+        xs = torch.empty((4, cfg.d), dtype=torch.int16, device="cuda")
+        bs = torch.empty((cfg.L, cfg.E), dtype=torch.float32, device="cuda")
+        out = torch.empty((cfg.L, 4, cfg.d), dtype=torch.int16, device="cuda")
+
+        def body():
+            st.set_router_bias(-1, bs)
+            for l in range(cfg.L):
+                st.forward(l, xs, out[l])
+
+        g = None
+        if use_graph:
+            xs.copy_(to_dev_bf16(steps[0][0]))
+            bs.copy_(torch.from_numpy(steps[0][1]).cuda())
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                body()
+        outs = []
+        for x, b in steps:
+            xs.copy_(to_dev_bf16(x))
+            bs.copy_(torch.from_numpy(b).cuda())
+            if use_graph:
+                g.replay()
+            else:
+                body()
+            torch.cuda.synchronize()
+            outs.append(out.cpu().numpy().copy())
+        state = st.cache_state()
+        stats = st.stats()
+        st.close()
+        return outs, state, stats
+
+    eager, st_e, s_e = run(False)
+    graph, st_g, s_g = run(True)
+    for a, b in zip(eager, graph):
+        np.testing.assert_array_equal(a, b)
+    for a, b in zip(st_e, st_g):
+        np.testing.assert_array_equal(np.asarray(a), np.asarray(b))
+    assert s_e["misses"] == s_g["misses"] > 0 and s_e["hits"] == s_g["hits"]
