@@ -41,6 +41,10 @@ WORKLOADS = {
                    batches=(1, 4, 16), headline_b=1),
     "prefill8": dict(L=8, E=256, k=6, d=4096, d_ff=2048, n_slots=16, shared=0,
                      tokens=(4096, 16384)),
+    "policy": dict(L=24, E=128, k=8, d=2048, d_ff=768, n_slots=768, zipf=1.1, shared=0,
+                   batches=(1, 16), steps=2000, refresh=500),
+    "elastic": dict(L=24, E=128, k=8, d=2048, d_ff=768, n_slots=768, zipf=1.1, shared=0,
+                    steps=10000, phase=1000, resizes=((3500, 307), (6500, 1228))),
 }
 SEED = 0
 
@@ -519,6 +523,135 @@ def run_prefill(args, wl, rank, world):
 
 
 # ----------------------------------------------------------------------------------------
+# placement-policy replay
+# ----------------------------------------------------------------------------------------
+def run_policy(args, wl, rank, world):
+    """Miss rates of the device LRU against a static layer split and a hot set refreshed every
+    `refresh` steps, at the same capacity, on the decode trace the CUDA path routes."""
+    import torch
+    from expert_cached_routed_router_b300.policy import RefreshedHotSet, StaticLayerSplit, miss_rate
+    seed = SEED + rank
+    pool = build_pool(wl, seed)
+    L, E, k = wl["L"], wl["E"], wl["k"]
+    n = wl["steps"] if args.steps == 200 else args.steps
+    res = {}
+    for b in wl["batches"]:
+        x_all, bias_all, _ = decode_trace(wl, b, n, seed)
+        st = make_stack(wl, pool, seed, max_tokens=16)
+        out = torch.empty((b, wl["d"]), dtype=torch.int16, device="cuda")
+        static = StaticLayerSplit(L, E, wl["n_slots"])
+        hot = RefreshedHotSet(L, E, wl["n_slots"], wl["refresh"])
+        for t in range(n):
+            static.step_begin(t)
+            hot.step_begin(t)
+            st.set_router_bias(-1, bias_all[t])
+            for l in range(L):
+                st.forward(l, x_all[t], out)
+                idx, _, _ = st.routing(b)
+                static.access(l, idx.ravel())
+                hot.access(l, idx.ravel())
+        s = st.stats()
+        st.close()
+        res[str(b)] = {"lru_miss_rate": round(s["misses"] / max(1, s["hits"] + s["misses"]), 4),
+                       "static_layer_split_miss_rate": round(miss_rate(static), 4),
+                       "refreshed_hot_set_miss_rate": round(miss_rate(hot), 4),
+                       "accesses": s["hits"] + s["misses"]}
+    return {"metric": "decode expert miss rate by placement policy (same capacity, same trace)",
+            "value": res[str(wl["batches"][0])]["lru_miss_rate"], "unit": "fraction",
+            "higher_is_better": False, "n_gpus": world, "steps": n, "warmup": 0,
+            "data": "synthetic",
+            "config": {"workload": "policy", "layers": L, "experts": E, "top_k": k,
+                       "capacity": wl["n_slots"], "refresh_steps": wl["refresh"],
+                       "by_batch": res}}
+
+
+# ----------------------------------------------------------------------------------------
+# elastic-cache stress
+# ----------------------------------------------------------------------------------------
+def run_elastic(args, wl, rank, world):
+    """10,000 decode steps of the 24-layer shapes: b = 1 in the first half of every block of
+    1,000 steps and b = 8 in the second, the popularity order switching between two disjoint
+    Zipf orders every 1,000 steps, and ft_cache_resize at the safe points before steps 3,500
+    (768 -> 307 slots) and 6,500 (307 -> 1,228).  Each batch size runs as its own CUDA graph."""
+    import torch
+    import ft_synth
+    import ft_synth.gpu as sg
+    seed = SEED + rank
+    pool = build_pool(wl, seed)
+    L, E, d = wl["L"], wl["E"], wl["d"]
+    n = min(wl["steps"], args.steps) if args.steps != 200 else wl["steps"]
+    gen = ft_synth.DriftingZipfBias(seed, L, E, s=wl["zipf"], phase_len=wl["phase"])
+    bias = np.empty((n, L, E), np.float32)
+    for t in range(n):
+        gen.advance()
+        for l in range(L):
+            bias[t, l] = gen.bias(l)
+    bias_d = torch.from_numpy(bias).cuda()
+    batch = [1 if (t % 1000) < 500 else 8 for t in range(n)]
+    x = {b: torch.empty((n, b, d), dtype=torch.int16, device="cuda") for b in (1, 8)}
+    for b in (1, 8):
+        sg.activations_device(x[b].data_ptr(), seed, [1_000_000 * b + t for t in range(n)], b, d,
+                              torch.cuda.current_stream().cuda_stream)
+    st = make_stack(wl, pool, seed, max_tokens=16)
+    xs = {b: torch.empty((b, d), dtype=torch.int16, device="cuda") for b in (1, 8)}
+    bs = torch.empty((L, E), dtype=torch.float32, device="cuda")
+    out = {b: torch.empty((L, b, d), dtype=torch.int16, device="cuda") for b in (1, 8)}
+    graphs = {}
+    for b in (1, 8):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            st.set_router_bias(-1, bs)
+            for l in range(L):
+                st.forward(l, xs[b], out[b][l])
+        graphs[b] = g
+    resizes = dict(wl["resizes"])
+    phase_stats = []
+    resize_ms = []
+    tokens = 0
+    torch.cuda.synchronize()
+    barrier(world)
+    t0 = time.perf_counter()
+    s_prev = st.stats()
+    for t in range(n):
+        if t in resizes:
+            r0 = time.perf_counter()
+            st.resize(resizes[t])
+            resize_ms.append((t, resizes[t], (time.perf_counter() - r0) * 1e3))
+            # the captured decode graphs stay valid: their kernels find the new slot storage
+            # through the library's device-side cache descriptor
+        b = batch[t]
+        xs[b].copy_(x[b][t])
+        bs.copy_(bias_d[t])
+        graphs[b].replay()
+        tokens += b
+        if (t + 1) % 500 == 0:
+            s = st.stats()
+            dh, dm = s["hits"] - s_prev["hits"], s["misses"] - s_prev["misses"]
+            phase_stats.append(dict(steps=f"{t - 499}-{t}", b=b, hit_rate=round(dh / max(1, dh + dm), 4),
+                                    n_slots=s["n_slots"]))
+            s_prev = s
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    barrier(world)
+    wall = max_over_ranks(wall, world)
+    s = st.stats()
+    assert s["status"] == 0, s
+    st.close()
+    return {
+        "metric": "MoE-layer tokens/s (elastic-cache stress trace, b=1/8, resizes)",
+        "value": round(world * tokens / wall, 2), "unit": "tokens/s", "n_gpus": world,
+        "steps": n, "warmup": 0, "ms_per_step": round(wall * 1e3 / n, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": "elastic", "layers": L, "d": d, "d_ff": wl["d_ff"], "experts": E,
+                   "top_k": wl["k"], "slots": [768, 307, 1228], "resize_ms": resize_ms,
+                   "hit_rate_by_500_steps": phase_stats, "hits": s["hits"],
+                   "misses": s["misses"], "evictions": s["evictions"],
+                   "timing": "host wall clock around the whole trace (includes the resizes)"},
+    }
+
+
+# ----------------------------------------------------------------------------------------
 # reference arm: the CPU oracle on the same workload
 # ----------------------------------------------------------------------------------------
 def run_reference(args, wl, rank, world):
@@ -607,6 +740,10 @@ def main():
     ftm.load_library()
     if args.workload == "prefill8":
         line = run_prefill(args, wl, rank, world)
+    elif args.workload == "elastic":
+        line = run_elastic(args, wl, rank, world)
+    elif args.workload == "policy":
+        line = run_policy(args, wl, rank, world)
     else:
         line = run_decode(args, wl, rank, world)
     if rank == 0:

@@ -45,6 +45,17 @@ struct DevCounters {
   int pad[2];
 };
 
+// Where the cache's slot state lives.  Kept in device memory and read by the kernels on
+// every call, so that a graph captured before ft_cache_resize (which reallocates the slot
+// storage) stays valid after it.
+struct CacheDesc {
+  uint16_t *slots;              // [n_slots][entry]
+  int32_t *owner;               // [n_slots]
+  unsigned long long *stamps;   // [n_slots]
+  int n_slots;
+  int pad;
+};
+
 // One group of rows of the expert FFN: the rows q0 .. q0+count-1 of the permuted
 // activations all use the weights of one complete entry W (W_gate | W_up | W_down).
 struct WorkItem {
@@ -72,11 +83,8 @@ struct ControlArgs {
   WorkItem *work;       // [E + 1]
   // cache (decode mode); null slot_table selects prefill mode
   int32_t *slot_table;  // [L][E]
-  int32_t *owner;       // [n_slots]
-  unsigned long long *stamps;  // [n_slots]
-  int n_slots;
+  const CacheDesc *cache;      // slot storage, owners, stamps, capacity (device)
   int32_t *fills;       // [max_fill][3]
-  const uint16_t *slots;       // slot storage
   const uint16_t *buffer;      // prefill: E entries of this layer
   const uint16_t *shared;      // shared entry of this layer or null
   size_t entry_elems;

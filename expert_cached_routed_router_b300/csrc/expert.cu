@@ -30,13 +30,15 @@ __device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f +
 // ---------------------------------------------------------------------------------------
 constexpr int kFillU = 8;
 
-__global__ void __launch_bounds__(512) k_fill(const uint4 *__restrict__ pool, uint4 *slots,
+__global__ void __launch_bounds__(512) k_fill(const uint4 *__restrict__ pool,
+                                              const CacheDesc *__restrict__ cache,
                                               const int32_t *__restrict__ fills,
                                               const DevCounters *__restrict__ ctr,
                                               size_t entry_vec, int E) {
   pdl_trigger();
   pdl_wait();
   const int n = ctr->n_fill;
+  uint4 *slots = reinterpret_cast<uint4 *>(cache->slots);
   const size_t stride = (size_t)gridDim.x * blockDim.x;
   const size_t t0 = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
   for (int f = 0; f < n; ++f) {
@@ -55,11 +57,11 @@ __global__ void __launch_bounds__(512) k_fill(const uint4 *__restrict__ pool, ui
   }
 }
 
-void launch_fill(const uint16_t *pool_dev, uint16_t *slots, const int32_t *fills,
+void launch_fill(const uint16_t *pool_dev, const CacheDesc *cache, const int32_t *fills,
                  DevCounters *ctr, size_t entry_bytes, int E, int max_fill, cudaStream_t s) {
   (void)max_fill;
-  launch_pdl(k_fill, dim3(148), dim3(512), 0, s, reinterpret_cast<const uint4 *>(pool_dev),
-             reinterpret_cast<uint4 *>(slots), fills, (const DevCounters *)ctr, entry_bytes / 16, E);
+  launch_pdl(k_fill, dim3(148), dim3(512), 0, s, reinterpret_cast<const uint4 *>(pool_dev), cache,
+             fills, (const DevCounters *)ctr, entry_bytes / 16, E);
 }
 
 // ---------------------------------------------------------------------------------------
@@ -76,23 +78,34 @@ void launch_fill(const uint16_t *pool_dev, uint16_t *slots, const int32_t *fills
 // ---------------------------------------------------------------------------------------
 constexpr int kGemvWarps = 8;            // consumer warps
 constexpr int kGemvThreads = (kGemvWarps + 1) * 32;
-constexpr int kMaxStages = 12;
+constexpr int kMaxStagesPerWarp = 4;
 constexpr uint32_t kRingBytes = 192u << 10;  // all stages together
 
-// Stage size: 16 KB, or larger when one gate+up row pair (4*d bytes) or one W_down row needs it.
-static uint32_t stage_bytes_for(uint32_t min_bytes) {
-  uint32_t b = 16u << 10;
-  while (b < min_bytes) b <<= 1;
-  return b;
+// Stages per consumer warp for a ring of `ring_bytes` (at least one).
+__host__ __device__ __forceinline__ int stages_per_warp(uint32_t ring_bytes, uint32_t stage_bytes) {
+  int s = (int)(ring_bytes / (stage_bytes * kGemvWarps));
+  return s < 1 ? 1 : (s > kMaxStagesPerWarp ? kMaxStagesPerWarp : s);
 }
 
+// The ring: consumer warp w owns stages w*spw .. w*spw+spw-1 and takes this CTA's tasks
+// w, w+8, w+16, ...; its j-th task uses stage w*spw + (j % spw) for the (j / spw)-th time.  A
+// stage therefore has one consumer that waits on its phases strictly in order, so a parity
+// wait can never match an older phase.
 struct RingSmem {
   uint8_t *base;
   uint32_t stage_bytes;
-  int n;  // stages
+  int spw;  // stages per consumer warp
   uint64_t *full;
   uint64_t *empty;
   __device__ __forceinline__ uint8_t *stage(int s) const { return base + (size_t)s * stage_bytes; }
+  __device__ __forceinline__ int n() const { return spw * kGemvWarps; }
+  // stage and use count of this CTA's it-th task
+  __device__ __forceinline__ void slot_of(long it, int &s, long &use) const {
+    const int w = (int)(it % kGemvWarps);
+    const long j = it / kGemvWarps;
+    s = w * spw + (int)(j % spw);
+    use = j / spw;
+  }
 };
 
 // Carve the dynamic shared memory: [x staging | stages | barriers].
@@ -101,20 +114,20 @@ __device__ __forceinline__ RingSmem ring_layout(uint8_t *smem, size_t x_bytes, u
   RingSmem r;
   r.base = smem + ((x_bytes + 127) & ~(size_t)127);
   r.stage_bytes = stage_bytes;
-  r.n = (int)min((uint32_t)kMaxStages, ring_bytes / stage_bytes);
-  r.full = reinterpret_cast<uint64_t *>(r.base + (size_t)r.n * stage_bytes);
-  r.empty = r.full + r.n;
+  r.spw = stages_per_warp(ring_bytes, stage_bytes);
+  r.full = reinterpret_cast<uint64_t *>(r.base + (size_t)r.n() * stage_bytes);
+  r.empty = r.full + r.n();
   return r;
 }
 
 static size_t ring_smem_bytes(size_t x_bytes, uint32_t stage_bytes, uint32_t ring_bytes) {
-  const int n = (int)std::min((uint32_t)kMaxStages, ring_bytes / stage_bytes);
+  const int n = stages_per_warp(ring_bytes, stage_bytes) * kGemvWarps;
   return ((x_bytes + 127) & ~(size_t)127) + (size_t)n * stage_bytes + 2 * n * 8;
 }
 
 __device__ __forceinline__ void ring_init(RingSmem &r) {
   if (threadIdx.x == 0) {
-    for (int s = 0; s < r.n; ++s) {
+    for (int s = 0; s < r.n(); ++s) {
       mbar_init(&r.full[s], 1);
       mbar_init(&r.empty[s], 1);
     }
@@ -122,40 +135,48 @@ __device__ __forceinline__ void ring_init(RingSmem &r) {
   }
 }
 
-// Producer side of the ring (one thread): for each of this CTA's tasks, wait for a free
-// stage and issue the bulk copies that `issue(task, stage_ptr, bar)` describes.  Returns
-// false on a timeout.  At the end it waits for its copies in flight.
+// Producer side of the ring (one thread): for each of this CTA's tasks, wait until the
+// task's stage has been released by its previous use and issue the bulk copies that
+// `issue(task, stage_ptr, bar)` describes.  Returns false on a timeout.  At the end it waits
+// for its copies in flight.
 template <typename Issue>
 __device__ __forceinline__ bool ring_produce(RingSmem &r, long n_tasks, Issue issue) {
   long it = 0;
   bool ok = true;
   for (long task = blockIdx.x; task < n_tasks; task += gridDim.x, ++it) {
-    const int s = (int)(it % r.n);
-    const uint32_t ph = (uint32_t)((it / r.n) & 1);
-    if (it >= r.n && !mbar_wait(&r.empty[s], ph ^ 1u)) {
+    int s;
+    long use;
+    r.slot_of(it, s, use);
+    if (use > 0 && !mbar_wait(&r.empty[s], (uint32_t)((use - 1) & 1))) {
       ok = false;
       break;
     }
     issue(task, r.stage(s), &r.full[s]);
   }
-  // drain: the copies of the last min(it, n) tasks may still be in flight
-  for (long i = (it > r.n ? it - r.n : 0); i < it; ++i)
-    mbar_wait(&r.full[i % r.n], (uint32_t)((i / r.n) & 1));
+  // drain: the copies of the last tasks (at most one in flight per stage)
+  const long n = r.n();
+  for (long i = (it > n ? it - n : 0); i < it; ++i) {
+    int s;
+    long use;
+    r.slot_of(i, s, use);
+    mbar_wait(&r.full[s], (uint32_t)(use & 1));
+  }
   return ok;
 }
 
 // Consumer side: consumer warp w takes this CTA's tasks w, w+8, ... whole; for each it waits
 // for the task's stage, runs `use`, and releases the stage.
 template <typename Use>
-__device__ __forceinline__ bool ring_consume(RingSmem &r, long n_tasks, Use use) {
+__device__ __forceinline__ bool ring_consume(RingSmem &r, long n_tasks, Use fn) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   long it = 0;
   for (long task = blockIdx.x; task < n_tasks; task += gridDim.x, ++it) {
     if ((int)(it % kGemvWarps) != warp) continue;
-    const int s = (int)(it % r.n);
-    const uint32_t ph = (uint32_t)((it / r.n) & 1);
-    if (!mbar_wait(&r.full[s], ph)) return false;
-    use(task, r.stage(s));
+    int s;
+    long use;
+    r.slot_of(it, s, use);
+    if (!mbar_wait(&r.full[s], (uint32_t)(use & 1))) return false;
+    fn(task, r.stage(s));
     __syncwarp();
     if (lane == 0) mbar_arrive(&r.empty[s]);
   }
@@ -223,21 +244,32 @@ __global__ void __launch_bounds__(kGemvThreads, 1) k_gateup_tma(
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   bool ok = true;
   if (warp == kGemvWarps) {
-    if (lane == 0)
+    if (lane == 0) {
+      int cu = -1;
+      const uint16_t *W = nullptr;
       ok = ring_produce(r, n_tasks, [&](long task, uint8_t *st, uint64_t *bar) {
         const int u = (int)(task / n_jb), j0 = (int)(task - (long)u * n_jb) * R;
         const int rows = min(R, d_ff - j0);
         const uint32_t bytes = (uint32_t)rows * d * 2;
-        const uint16_t *W = work[u].W;
+        if (u != cu) {  // consecutive tasks mostly stay on one item
+          cu = u;
+          W = work[u].W;
+        }
         mbar_arrive_expect_tx(bar, 2 * bytes);
         bulk_g2s(st, W + (size_t)j0 * d, bytes, bar);
         bulk_g2s(st + (size_t)R * d * 2, W + (size_t)(d_ff + j0) * d, bytes, bar);
       });
+    }
   } else {
+    int cu = -1;
+    WorkItem wi{};
     ok = ring_consume(r, n_tasks, [&](long task, const uint8_t *st) {
       const int u = (int)(task / n_jb), j0 = (int)(task - (long)u * n_jb) * R;
       const int rows = min(R, d_ff - j0);
-      const WorkItem wi = work[u];
+      if (u != cu) {
+        cu = u;
+        wi = work[u];
+      }
       const int c = wi.count;
       for (int rr = 0; rr < rows; ++rr) {
         const uint4 *g = reinterpret_cast<const uint4 *>(st + (size_t)rr * d * 2);
@@ -319,19 +351,31 @@ __global__ void __launch_bounds__(kGemvThreads, 1) k_down_tma(
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   bool ok = true;
   if (warp == kGemvWarps) {
-    if (lane == 0)
+    if (lane == 0) {
+      int cu = -1;
+      const uint16_t *W = nullptr;
       ok = ring_produce(r, n_tasks, [&](long task, uint8_t *st, uint64_t *bar) {
         const int u = (int)(task / n_ib), i0 = (int)(task - (long)u * n_ib) * R;
         const int rows = min(R, d - i0);
         const uint32_t bytes = (uint32_t)rows * d_ff * 2;
+        if (u != cu) {
+          cu = u;
+          W = work[u].W;
+        }
         mbar_arrive_expect_tx(bar, bytes);
-        bulk_g2s(st, work[u].W + (size_t)2 * d_ff * d + (size_t)i0 * d_ff, bytes, bar);
+        bulk_g2s(st, W + (size_t)2 * d_ff * d + (size_t)i0 * d_ff, bytes, bar);
       });
+    }
   } else {
+    int cu = -1;
+    WorkItem wi{};
     ok = ring_consume(r, n_tasks, [&](long task, const uint8_t *st) {
       const int u = (int)(task / n_ib), i0 = (int)(task - (long)u * n_ib) * R;
       const int rows = min(R, d - i0);
-      const WorkItem wi = work[u];
+      if (u != cu) {
+        cu = u;
+        wi = work[u];
+      }
       const int c = wi.count;
       for (int t0 = 0; t0 < c; t0 += 4) {
         const int n = min(4, c - t0);
@@ -384,13 +428,14 @@ static void allow_smem(K kern, size_t smem) {
 void launch_gateup_gemv(const WorkItem *work, DevCounters *ctr, int max_work, const uint16_t *x,
                         const int32_t *tok, uint16_t *h, int T, int d, int d_ff, cudaStream_t s) {
   (void)max_work;
-  const uint32_t sb = stage_bytes_for(4u * d);
-  const int R = std::max(1, std::min(d_ff, (int)(sb / (4u * d))));
-  // x next to the ring when at least 4 stages still fit in 224 KB
-  const size_t xb = (size_t)T * d * 2;
-  const bool xs = xb + 4 * (size_t)sb <= (224u << 10);
-  const uint32_t ring = xs ? (uint32_t)std::min<size_t>(kRingBytes, (224u << 10) - ((xb + 127) & ~(size_t)127))
-                           : kRingBytes;
+  // one stage per consumer warp holding R gate+up row pairs (R <= 4), as many as fit next to
+  // x (kept in shared memory when a one-pair stage per warp still fits in 224 KB)
+  const uint32_t unit = 4u * d;
+  const size_t xb = (size_t)T * d * 2, xr = (xb + 127) & ~(size_t)127;
+  const bool xs = xr + (size_t)kGemvWarps * unit <= (224u << 10);
+  const uint32_t ring = xs ? (uint32_t)std::min<size_t>(kRingBytes, (224u << 10) - xr) : kRingBytes;
+  const int R = std::max(1, std::min({d_ff, 4, (int)(ring / kGemvWarps / unit)}));
+  const uint32_t sb = (uint32_t)R * unit;
   const size_t smem = ring_smem_bytes(xs ? xb : 0, sb, ring);
   auto go = [&](auto kern) {
     allow_smem(kern, smem);
@@ -455,8 +500,9 @@ void launch_down_gemv(const WorkItem *work, DevCounters *ctr, int max_work, cons
                       const int32_t *inv, const float *w, float *y, uint16_t *out, int T, int k,
                       int d, int d_ff, int shared, cudaStream_t s) {
   (void)max_work;
-  const uint32_t sb = stage_bytes_for(2u * d_ff);
-  const int R = std::max(1, std::min({d, kDownRows, (int)(sb / (2u * d_ff))}));
+  const uint32_t unit = 2u * d_ff;
+  const int R = std::max(1, std::min({d, kDownRows, (int)(kRingBytes / kGemvWarps / unit)}));
+  const uint32_t sb = (uint32_t)R * unit;
   const size_t smem = ring_smem_bytes(0, sb, kRingBytes);
   allow_smem(k_down_tma, smem);
   launch_pdl(k_down_tma, dim3(sm_count()), dim3(kGemvThreads), smem, s, work, ctr, h, y, d, d_ff,

@@ -67,6 +67,7 @@ struct ft_moe {
   int32_t *owner = nullptr;
   unsigned long long *stamps = nullptr;
   DevCounters *ctr = nullptr;
+  CacheDesc *cache = nullptr;  // device copy of {slots, owner, stamps, n_slots}
   float *logits = nullptr;
   int32_t *idx = nullptr;
   float *w = nullptr;
@@ -229,17 +230,22 @@ ControlArgs control_args(ft_moe *h, int layer, int T, bool decode, const uint16_
   a.wq = h->wq;
   a.work = h->work;
   a.slot_table = decode ? h->slot_table : nullptr;
-  a.owner = h->owner;
-  a.stamps = h->stamps;
-  a.n_slots = h->n_slots;
+  a.cache = h->cache;
   a.fills = h->fills;
-  a.slots = h->slots;
   a.buffer = buffer;
   a.shared = h->n_shared ? h->shared + (size_t)layer * h->entry_elems : nullptr;
   a.entry_elems = h->entry_elems;
   a.ctr = h->ctr;
   a.d = h->d;
   return a;
+}
+
+// Publish the current slot storage to the device-side descriptor the kernels read.
+int upload_cache_desc(ft_moe *h) {
+  CacheDesc d{h->slots, h->owner, h->stamps, h->n_slots, 0};
+  cudaError_t e = cudaMemcpy(h->cache, &d, sizeof(d), cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) return fail(FT_ERR_CUDA, "cache descriptor: %s", cudaGetErrorString(e));
+  return FT_OK;
 }
 
 // Tensor maps for the tcgen05 GEMMs over `buffer` (n_entries complete entries).
@@ -340,8 +346,9 @@ int ft_moe_create(int L, int E, int k, int d, int d_ff, int n_slots, const ft_mo
   if (L < 1 || E < 1 || E > kMaxE || k < 1 || k > E || k > kMaxK)
     return fail(FT_ERR_INVALID, "need L >= 1, 1 <= k <= E <= %d, k <= %d (got L=%d E=%d k=%d)",
                 kMaxE, kMaxK, L, E, k);
-  if (d < 128 || d % 128 || d > 8192 || d_ff < 128 || d_ff % 128 || d_ff > 8192)
-    return fail(FT_ERR_INVALID, "need d, d_ff multiples of 128 in [128, 8192] (got %d, %d)", d,
+  if (d < 128 || d % 128 || d > 4096 || d_ff < 128 || d_ff % 128 || d_ff > 8192)
+    return fail(FT_ERR_INVALID,
+                "need d in [128, 4096] and d_ff in [128, 8192], multiples of 128 (got %d, %d)", d,
                 d_ff);
   if (n_slots < 1) return fail(FT_ERR_INVALID, "n_slots must be >= 1 (got %d)", n_slots);
   ft_moe_opts o{0, 1, 4096, 0};
@@ -376,6 +383,7 @@ int ft_moe_create(int L, int E, int k, int d, int d_ff, int n_slots, const ft_mo
   if (o.n_shared) A(alloc_n(h, &h->shared, (size_t)L * h->entry_elems));
   A(alloc_n(h, &h->slot_table, (size_t)L * E));
   A(alloc_n(h, &h->ctr, 1));
+  A(alloc_n(h, &h->cache, 1));
   A(alloc_n(h, &h->logits, T * E));
   A(alloc_n(h, &h->idx, P));
   A(alloc_n(h, &h->w, P));
@@ -418,6 +426,7 @@ int ft_moe_create(int L, int E, int k, int d, int d_ff, int n_slots, const ft_mo
     if (e != cudaSuccess) rc = fail(FT_ERR_CUDA, "initialisation: %s", cudaGetErrorString(e));
   }
   if (rc == FT_OK) rc = build_maps(h, &h->maps_slots, h->slots, n_slots);
+  if (rc == FT_OK) rc = upload_cache_desc(h);
   if (rc != FT_OK) {
     free_all(h);
     delete h;
@@ -550,7 +559,7 @@ int ft_moe_forward(ft_moe *h, int layer, const void *x, int T, void *out, ft_str
   route_layer(h, layer, xb, T, true, nullptr, s);
   {
     ProfScope p(h, FT_PROF_FILL, s);
-    launch_fill(h->pool_dev, h->slots, h->fills, h->ctr, h->entry_bytes, h->E,
+    launch_fill(h->pool_dev, h->cache, h->fills, h->ctr, h->entry_bytes, h->E,
                 std::min(h->E, T * h->k), s);
   }
   experts_layer(h, xb, T, static_cast<uint16_t *>(out), h->maps_slots, layer, s);
@@ -749,6 +758,7 @@ int ft_cache_resize(ft_moe *h, int n_new) {
   h->owner = nowner;
   h->stamps = nstamps;
   h->n_slots = n_new;
+  if (int r = upload_cache_desc(h)) return r;
   if (int r = build_maps(h, &h->maps_slots, h->slots, n_new)) return r;
   DevCounters c{};
   FT_CUDA(cudaMemcpy(&c, h->ctr, sizeof(c), cudaMemcpyDeviceToHost));

@@ -31,7 +31,7 @@ void launch_route_decode(const uint16_t *x, const uint16_t *wr, const float *bia
                          const ControlArgs &a, cudaStream_t s);
 
 // Copy the fill list's entries from the mapped host pool into their slots.
-void launch_fill(const uint16_t *pool_dev, uint16_t *slots, const int32_t *fills,
+void launch_fill(const uint16_t *pool_dev, const CacheDesc *cache, const int32_t *fills,
                  DevCounters *ctr, size_t entry_bytes, int E, int max_fill, cudaStream_t s);
 
 // Decode expert FFN (T <= kGemvMaxTokens): gate/up GEMV + SwiGLU into h; down GEMV into the

@@ -426,8 +426,10 @@ __device__ __forceinline__ void control_body(const ControlArgs &a, int perm_read
   }
 
   int slot_of = -1;
+  CacheDesc cd{};
+  if (a.slot_table) cd = *a.cache;
   if (a.slot_table) {
-    if (n_touched > a.n_slots) {
+    if (n_touched > cd.n_slots) {
       if (tid == 0) {
         set_status(a.ctr, FT_ERR_CAPACITY);
         a.ctr->call_status = FT_ERR_CAPACITY;
@@ -446,16 +448,16 @@ __device__ __forceinline__ void control_body(const ControlArgs &a, int perm_read
     const int mrank = block_incl_scan(miss ? 1 : 0, s_warp, &total) - (miss ? 1 : 0);
     const int n_miss = total;
     if (hit) {
-      if (cur < a.n_slots)
-        a.stamps[cur] = tick0 + 1 + (unsigned long long)hrank;
+      if (cur < cd.n_slots)
+        cd.stamps[cur] = tick0 + 1 + (unsigned long long)hrank;
       else
         set_status(a.ctr, FT_ERR_INVALID);
     }
     // the n_miss lowest free slots
     int n_free = 0;
-    for (int base = 0; base < a.n_slots; base += 1024) {
+    for (int base = 0; base < cd.n_slots; base += 1024) {
       const int s = base + tid;
-      const bool f = s < a.n_slots && a.owner[s] < 0;
+      const bool f = s < cd.n_slots && cd.owner[s] < 0;
       const int r = block_incl_scan(f ? 1 : 0, s_warp, &total) - (f ? 1 : 0);
       if (f && n_free + r < n_miss) s_list[n_free + r] = s;
       n_free += total;
@@ -464,23 +466,23 @@ __device__ __forceinline__ void control_body(const ControlArgs &a, int perm_read
     const int nv = n_miss > n_free ? n_miss - n_free : 0;
     if (nv > 0) {
       // eviction keys: (stamp, slot) of occupied slots not touched in this call
-      const bool in_smem = a.n_slots <= kStampSmem;
+      const bool in_smem = cd.n_slots <= kStampSmem;
       if (in_smem) {
-        for (int s = tid; s < a.n_slots; s += 1024) {
-          const unsigned long long st = a.stamps[s];
-          s_key[s] = (a.owner[s] >= 0 && st <= tick0) ? st : ~0ull;
+        for (int s = tid; s < cd.n_slots; s += 1024) {
+          const unsigned long long st = cd.stamps[s];
+          s_key[s] = (cd.owner[s] >= 0 && st <= tick0) ? st : ~0ull;
         }
       }
       __syncthreads();
-      for (int s = tid; s < a.n_slots; s += 1024) {
+      for (int s = tid; s < cd.n_slots; s += 1024) {
         const unsigned long long ks =
-            in_smem ? s_key[s] : ((a.owner[s] >= 0 && a.stamps[s] <= tick0) ? a.stamps[s] : ~0ull);
+            in_smem ? s_key[s] : ((cd.owner[s] >= 0 && cd.stamps[s] <= tick0) ? cd.stamps[s] : ~0ull);
         if (ks == ~0ull) continue;
         int rank = 0;
-        for (int s2 = 0; s2 < a.n_slots && rank < nv; ++s2) {
+        for (int s2 = 0; s2 < cd.n_slots && rank < nv; ++s2) {
           const unsigned long long k2 =
               in_smem ? s_key[s2]
-                      : ((a.owner[s2] >= 0 && a.stamps[s2] <= tick0) ? a.stamps[s2] : ~0ull);
+                      : ((cd.owner[s2] >= 0 && cd.stamps[s2] <= tick0) ? cd.stamps[s2] : ~0ull);
           rank += (k2 < ks || (k2 == ks && s2 < s)) ? 1 : 0;
         }
         if (rank < nv) s_victim[rank] = s;
@@ -491,12 +493,12 @@ __device__ __forceinline__ void control_body(const ControlArgs &a, int perm_read
       const int m = mrank;
       const int slot = (m < n_free) ? s_list[m] : s_victim[m - n_free];
       if (m >= n_free) {
-        const int ev = a.owner[slot];
+        const int ev = cd.owner[slot];
         if (ev >= 0 && ev < a.L * E) a.slot_table[ev] = -1;
       }
-      a.owner[slot] = a.layer * E + tid;
+      cd.owner[slot] = a.layer * E + tid;
       table[tid] = slot;
-      a.stamps[slot] = tick0 + (unsigned long long)n_hit + 1ull + (unsigned long long)m;
+      cd.stamps[slot] = tick0 + (unsigned long long)n_hit + 1ull + (unsigned long long)m;
       a.fills[3 * m + 0] = slot;
       a.fills[3 * m + 1] = a.layer;
       a.fills[3 * m + 2] = tid;
@@ -520,7 +522,7 @@ __device__ __forceinline__ void control_body(const ControlArgs &a, int perm_read
   }
   if (touched) {
     WorkItem wi;
-    wi.W = (a.slot_table ? a.slots : a.buffer) + (size_t)slot_of * a.entry_elems;
+    wi.W = (a.slot_table ? cd.slots : a.buffer) + (size_t)slot_of * a.entry_elems;
     wi.q0 = s_off[tid];
     wi.count = s_cnt[tid];
     wi.expert = tid;

@@ -90,7 +90,8 @@ const char *ft_last_error(void);
  * Create a layer stack: L layers, E routed experts per layer, top-k routing, hidden size d,
  * expert FFN size d_ff, and a cache of n_slots complete (layer, expert) entries.
  * Requires 1 <= k <= E <= 1024, k <= 32, d % 128 == 0, d_ff % 128 == 0, 1 <= n_slots,
- * d <= 8192, d_ff <= 8192.
+ * d <= 4096 (a W_gate + W_up row pair must fit one 16 KB shared-memory stage per decode
+ * consumer warp), d_ff <= 8192.
  * One entry is 3*d*d_ff bf16: W_gate rows [d_ff][d], W_up rows [d_ff][d], W_down rows
  * [d][d_ff] (each row one output feature, contiguous over input features).  The library
  * allocates and owns all device state (router weights, slot storage, tables, scratch).
@@ -172,7 +173,10 @@ int ft_moe_prefill_timing(ft_moe *h, float *copy_ms, float *compute_ms, float *w
  * min(n_slots, occupied) most recently used entries (moved device-to-device into slots 0..
  * in descending stamp order, stamps kept), frees the old slot storage.  Never reads the
  * host pool.  FT_ERR_STATE while a stream capture is active; FT_ERR_OOM leaves the cache
- * exactly as it was.
+ * exactly as it was.  Graphs of decode calls (T <= 16) captured before a resize stay valid:
+ * their kernels find the slot storage through a device-side descriptor that the resize
+ * updates.  Graphs of calls with T > 16 hold tensor maps of the old storage and must be
+ * captured again.
  */
 int ft_cache_resize(ft_moe *h, int n_slots);
 

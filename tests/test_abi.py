@@ -43,6 +43,7 @@ def test_binding_has_the_c_names():
     (1, 16, 2, 256, 100, 16),      # d_ff not a multiple of 128
     (1, 16, 2, 256, 128, 0),       # no slots
     (1, 64, 40, 256, 128, 16),     # k > 32
+    (1, 16, 2, 8192, 128, 16),     # d > 4096
 ])
 def test_create_rejects_bad_shapes(args):
     with pytest.raises(ftm.FtError) as ei:

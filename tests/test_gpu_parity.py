@@ -221,7 +221,8 @@ def test_resize_allocation_failure_leaves_cache_intact(monkeypatch):
 
 def test_decode_step_graph_capture_matches_eager():
     """One decode step (several layers, shared cache) captured into a CUDA graph and replayed
-    gives the same outputs and the same cache state as the same calls run eagerly."""
+    gives the same outputs and the same cache state as the same calls run eagerly, also across
+    an elastic resize between two replays (the graph is not captured again)."""
     import torch
     cfg = Config(L=3, E=16, k=2, d=256, d_ff=128, n_slots=10, seed=10)
     gen = ft_synth.DriftingZipfBias(10, cfg.L, cfg.E, s=0.8, sigma_walk=0.3)
@@ -254,7 +255,9 @@ def test_decode_step_graph_capture_matches_eager():
             with torch.cuda.graph(g):
                 body()
         outs = []
-        for x, b in steps:
+        for i, (x, b) in enumerate(steps):
+            if i == 3:
+                st.resize(7)            # safe point between steps
             xs.copy_(to_dev_bf16(x))
             bs.copy_(torch.from_numpy(b).cuda())
             if use_graph:
