@@ -410,7 +410,7 @@ def run_decode(args, wl, rank, world):
     g = rl["gateup"]
     # DRAM bytes per launch of k_gateup_tma at b = 1 (8 touched experts) from the committed ncu
     # capture (profiles/decode_kernels_full_capture.md); only valid for that shape
-    traffic = 50.47e6 if (args.workload == "decode24" and b == 1) else None
+    traffic = 50.47e6 if (args.workload == "decode24" and b == 1) else None  # ncu, per launch
     roof = {"bound": "hbm", "kernel": "k_gateup_tma (gate/up + SwiGLU, decode)",
             "achieved": round(g["achieved"], 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
             "frac": round(g["achieved"] / pk["hbm_gbs"], 4), "traffic": traffic,
@@ -437,10 +437,9 @@ def run_decode(args, wl, rank, world):
         "cpu_baseline": cpu,
         "e2e": {"value": round(res["e2e_tok_s_all"], 2), "unit": "tokens/s",
                 "h2d_bytes_per_step": res["e2e"]["h2d"], "d2h_bytes_per_step": res["e2e"]["d2h"]},
-        # kernels per decode layer call: routing, fill, gate/up, down, combine (the "down"
-        # timing scope covers down + combine)
-        "gpu_launches": int((sum(v[1] for v in prof.values()) + prof["down"][1]) / prof_k
-                            * args.steps),
+        # kernels per decode layer call: routing, fill, gate/up, down, combine (one timing
+        # scope each)
+        "gpu_launches": int(sum(v[1] for v in prof.values()) / prof_k * args.steps),
         "clocks": res["clocks"],
     }
     return line

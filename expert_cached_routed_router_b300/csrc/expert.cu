@@ -497,8 +497,8 @@ __global__ void k_combine(const float *__restrict__ y, const float *__restrict__
 }
 
 void launch_down_gemv(const WorkItem *work, DevCounters *ctr, int max_work, const uint16_t *h,
-                      const int32_t *inv, const float *w, float *y, uint16_t *out, int T, int k,
-                      int d, int d_ff, int shared, cudaStream_t s) {
+                      float *y, int T, int d, int d_ff, cudaStream_t s) {
+  (void)T;
   (void)max_work;
   const uint32_t unit = 2u * d_ff;
   const int R = std::max(1, std::min({d, kDownRows, (int)(kRingBytes / kGemvWarps / unit)}));
@@ -507,9 +507,13 @@ void launch_down_gemv(const WorkItem *work, DevCounters *ctr, int max_work, cons
   allow_smem(k_down_tma, smem);
   launch_pdl(k_down_tma, dim3(sm_count()), dim3(kGemvThreads), smem, s, work, ctr, h, y, d, d_ff,
              R, sb, kRingBytes);
+}
+
+void launch_combine(const float *y, const float *w, const int32_t *inv, const DevCounters *ctr,
+                    uint16_t *out, int T, int k, int d, int shared, cudaStream_t s) {
   const int n = T * (d >> 3);
-  launch_pdl(k_combine, dim3((n + 255) / 256), dim3(256), 0, s, (const float *)y, w, inv,
-             (const DevCounters *)ctr, out, T, k, d, shared);
+  launch_pdl(k_combine, dim3((n + 255) / 256), dim3(256), 0, s, y, w, inv, ctr, out, T, k, d,
+             shared);
 }
 
 // ---------------------------------------------------------------------------------------

@@ -308,9 +308,12 @@ void experts_layer(ft_moe *h, const uint16_t *x, int T, uint16_t *out, const TcM
       ProfScope p(h, FT_PROF_GATEUP, s);
       launch_gateup_gemv(h->work, h->ctr, max_work, x, h->tok, h->hbuf, T, h->d, h->d_ff, s);
     }
-    ProfScope p(h, FT_PROF_DOWN, s);
-    launch_down_gemv(h->work, h->ctr, max_work, h->hbuf, h->inv, h->w, h->ybuf, out, T, h->k,
-                     h->d, h->d_ff, h->n_shared, s);
+    {
+      ProfScope p(h, FT_PROF_DOWN, s);
+      launch_down_gemv(h->work, h->ctr, max_work, h->hbuf, h->ybuf, T, h->d, h->d_ff, s);
+    }
+    ProfScope p(h, FT_PROF_OTHER, s);
+    launch_combine(h->ybuf, h->w, h->inv, h->ctr, out, T, h->k, h->d, h->n_shared, s);
   } else {
     const int rows = P + (h->n_shared ? T : 0);
     {

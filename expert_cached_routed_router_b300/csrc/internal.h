@@ -35,12 +35,13 @@ void launch_fill(const uint16_t *pool_dev, const CacheDesc *cache, const int32_t
                  DevCounters *ctr, size_t entry_bytes, int E, int max_fill, cudaStream_t s);
 
 // Decode expert FFN (T <= kGemvMaxTokens): gate/up GEMV + SwiGLU into h; down GEMV into the
-// fp32 per-row buffer y [(T*k + T)][d]; then the weighted combine into out.
+// fp32 per-row buffer y [(T*k + T)][d]; then the deterministic weighted combine into out.
 void launch_gateup_gemv(const WorkItem *work, DevCounters *ctr, int max_work, const uint16_t *x,
                         const int32_t *tok, uint16_t *h, int T, int d, int d_ff, cudaStream_t s);
 void launch_down_gemv(const WorkItem *work, DevCounters *ctr, int max_work, const uint16_t *h,
-                      const int32_t *inv, const float *w, float *y, uint16_t *out, int T, int k,
-                      int d, int d_ff, int shared, cudaStream_t s);
+                      float *y, int T, int d, int d_ff, cudaStream_t s);
+void launch_combine(const float *y, const float *w, const int32_t *inv, const DevCounters *ctr,
+                    uint16_t *out, int T, int k, int d, int shared, cudaStream_t s);
 
 // Grouped-GEMM expert FFN for larger T.
 void launch_gather_rows(const uint16_t *x, const int32_t *tok, uint16_t *xp, int rows, int d,
