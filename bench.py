@@ -13,7 +13,8 @@ more than L2 (126 MB), so no flush is needed.
 
 Other workloads: ``--workload large8`` (8 layers, d=4096, d_ff=2048, E=256, top-6 + shared
 expert, 640 slots = 30 GiB), ``--workload prefill8`` (prefill streaming, 8 layers, T=4096 and
-16384).
+16384), ``--workload prefill8_topup`` (the same prefill with the full 640-slot decode cache
+feeding the double buffer device -> device; only absent experts cross the host link).
 
 ``--impl reference`` times the CPU oracle (the slow, plain reference implementation) on the
 same workload; each step is one layer call of the b=1 trace.
@@ -41,6 +42,9 @@ WORKLOADS = {
                    batches=(1, 4, 16), headline_b=1),
     "prefill8": dict(L=8, E=256, k=6, d=4096, d_ff=2048, n_slots=16, shared=0,
                      tokens=(4096, 16384)),
+    # prefill top-up: the 640-slot (30 GiB) decode cache, full, feeds the double buffer
+    "prefill8_topup": dict(L=8, E=256, k=6, d=4096, d_ff=2048, n_slots=640, shared=0,
+                           tokens=(4096, 16384), topup=1),
     "policy": dict(L=24, E=128, k=8, d=2048, d_ff=768, n_slots=768, zipf=1.1, shared=0,
                    batches=(1, 16), steps=2000, refresh=500),
     "elastic": dict(L=24, E=128, k=8, d=2048, d_ff=768, n_slots=768, zipf=1.1, shared=0,
@@ -160,7 +164,8 @@ def make_stack(wl, pool, seed, max_tokens, n_slots=None):
     import ft_synth
     from expert_cached_routed_router_b300 import MoELayerStack
     st = MoELayerStack(wl["L"], wl["E"], wl["k"], wl["d"], wl["d_ff"],
-                       n_slots or wl["n_slots"], n_shared=wl["shared"], max_tokens=max_tokens)
+                       n_slots or wl["n_slots"], n_shared=wl["shared"], max_tokens=max_tokens,
+                       prefill_topup=wl.get("topup", 0))
     for l in range(wl["L"]):
         wr = ft_synth.router_weight(seed, l, wl["E"], wl["d"])
         st.load_router(l, torch.from_numpy(wr.view(np.int16)).cuda())
@@ -493,11 +498,13 @@ def run_prefill(args, wl, rank, world):
         gemm_ms = prof["gateup"][0] + prof["down"][0]
         tflops = flops / (gemm_ms / 1e3) / 1e12 if gemm_ms > 0 else 0.0
         overlap = (copy_ms + comp_ms - wall_ms) / max(1e-9, min(copy_ms, comp_ms))
+        h2d_b, d2d_b = st.prefill_bytes()
         per_T[T] = dict(ms_per_prefill=ms / K, tok_s=world * T * K / (ms / 1e3),
                         gemm_ms_per_layer=gemm_ms / L, gemm_tflops=tflops,
                         tc_frac=tflops / pk["bf16"], copy_ms=copy_ms / K,
                         compute_ms=comp_ms / K, wall_ms=wall_ms / K, overlap=overlap,
-                        h2d_gbs=L * wl["E"] * 3 * d * d_ff * 2 / (copy_ms / K / 1e3) / 1e9,
+                        h2d_gbs=h2d_b / (copy_ms / K / 1e3) / 1e9,
+                        h2d_gb_per_prefill=h2d_b / 1e9, d2d_gb_per_prefill=d2d_b / 1e9,
                         kernels_ms={c: v[0] for c, v in prof.items()}, clocks=clk.summary())
         st.close()
         del x, out
@@ -505,7 +512,8 @@ def run_prefill(args, wl, rank, world):
     Th = wl["tokens"][-1]
     r = per_T[Th]
     return {
-        "metric": f"MoE-layer prefill tokens/s (T={Th}, 8 layers streamed)",
+        "metric": f"MoE-layer prefill tokens/s (T={Th}, 8 layers streamed"
+                  + (", cache top-up)" if wl.get("topup") else ")"),
         "value": round(r["tok_s"], 1), "unit": "tokens/s", "n_gpus": world, "steps": K,
         "warmup": W, "ms_per_step": round(r["ms_per_prefill"], 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
@@ -737,7 +745,7 @@ def main():
     rank, world, _ = dist_setup(args)
     import expert_cached_routed_router_b300 as ftm
     ftm.load_library()
-    if args.workload == "prefill8":
+    if args.workload in ("prefill8", "prefill8_topup"):
         line = run_prefill(args, wl, rank, world)
     elif args.workload == "elastic":
         line = run_elastic(args, wl, rank, world)

@@ -24,7 +24,8 @@ ERROR_NAMES = {0: "FT_OK", 1: "FT_ERR_INVALID", 2: "FT_ERR_STATE", 3: "FT_ERR_CU
 EXPORTS = [
     "ft_last_error", "ft_moe_create", "ft_moe_destroy", "ft_moe_load_router",
     "ft_moe_set_router_bias", "ft_moe_load_pool", "ft_moe_load_shared", "ft_moe_forward",
-    "ft_moe_decode_host", "ft_moe_prefill_stream", "ft_moe_prefill_timing", "ft_cache_resize",
+    "ft_moe_decode_host", "ft_moe_prefill_stream", "ft_moe_prefill_bytes",
+    "ft_moe_prefill_timing", "ft_cache_resize",
     "ft_cache_stats", "ft_cache_stats_reset", "ft_moe_status", "ft_moe_get_routing",
     "ft_moe_get_logits", "ft_moe_get_perm", "ft_moe_get_cache_state", "ft_moe_get_fills",
     "ft_moe_get_dims", "ft_moe_profile", "ft_moe_profile_read", "ft_route_topk_noalloc",
@@ -41,7 +42,8 @@ class FtError(RuntimeError):
 
 class ft_moe_opts(ctypes.Structure):
     _fields_ = [("n_shared", ctypes.c_int), ("prewarm", ctypes.c_int),
-                ("max_tokens", ctypes.c_int), ("debug_checks", ctypes.c_int)]
+                ("max_tokens", ctypes.c_int), ("debug_checks", ctypes.c_int),
+                ("prefill_topup", ctypes.c_int)]
 
 
 class ft_cache_stats_t(ctypes.Structure):
@@ -81,6 +83,8 @@ def load_library(path: str = LIB_PATH):
         "ft_moe_forward": (I, [P, I, P, I, P, P]),
         "ft_moe_decode_host": (I, [P, I, I, P, I, P, P]),
         "ft_moe_prefill_stream": (I, [P, I, I, P, I, P, P]),
+        "ft_moe_prefill_bytes": (I, [P, ctypes.POINTER(ctypes.c_uint64),
+                                     ctypes.POINTER(ctypes.c_uint64)]),
         "ft_moe_prefill_timing": (I, [P, ctypes.POINTER(ctypes.c_float),
                                       ctypes.POINTER(ctypes.c_float),
                                       ctypes.POINTER(ctypes.c_float)]),
@@ -136,9 +140,9 @@ def _stream(stream) -> int | None:
 # -------- functions with the C names (marshalling only) ----------------------------------
 
 def ft_moe_create(L, E, k, d, d_ff, n_slots, n_shared=0, prewarm=1, max_tokens=4096,
-                  debug_checks=0) -> int:
+                  debug_checks=0, prefill_topup=0) -> int:
     lib = load_library()
-    opts = ft_moe_opts(n_shared, prewarm, max_tokens, debug_checks)
+    opts = ft_moe_opts(n_shared, prewarm, max_tokens, debug_checks, prefill_topup)
     h = ctypes.c_void_p()
     _check(lib.ft_moe_create(L, E, k, d, d_ff, n_slots, ctypes.byref(opts), ctypes.byref(h)))
     return h.value
@@ -176,6 +180,12 @@ def ft_moe_decode_host(h, layer0, n_layers, x_host, T, out_host, stream=None):
 def ft_moe_prefill_stream(h, layer0, n_layers, x, T, out, stream=None):
     _check(load_library().ft_moe_prefill_stream(h, layer0, n_layers, _ptr(x), T, _ptr(out),
                                                 _stream(stream)))
+
+
+def ft_moe_prefill_bytes(h):
+    a, b = ctypes.c_uint64(), ctypes.c_uint64()
+    _check(load_library().ft_moe_prefill_bytes(h, ctypes.byref(a), ctypes.byref(b)))
+    return a.value, b.value
 
 
 def ft_moe_prefill_timing(h):
@@ -285,12 +295,12 @@ class MoELayerStack:
     """One ft_moe handle: L routed-MoE layers sharing one LRU expert-slot cache."""
 
     def __init__(self, L, E, k, d, d_ff, n_slots, n_shared=0, prewarm=1, max_tokens=4096,
-                 debug_checks=0):
+                 debug_checks=0, prefill_topup=0):
         self.L, self.E, self.k, self.d, self.d_ff = L, E, k, d, d_ff
         self.n_shared = n_shared
         self.entry_elems = 3 * d * d_ff
         self.h = ft_moe_create(L, E, k, d, d_ff, n_slots, n_shared, prewarm, max_tokens,
-                               debug_checks)
+                               debug_checks, prefill_topup)
 
     def close(self):
         if self.h:
@@ -326,6 +336,10 @@ class MoELayerStack:
 
     def prefill_timing(self):
         return ft_moe_prefill_timing(self.h)
+
+    def prefill_bytes(self):
+        """(host -> device, slot -> buffer) bytes moved by the most recent prefill."""
+        return ft_moe_prefill_bytes(self.h)
 
     def resize(self, n_slots):
         ft_cache_resize(self.h, n_slots)

@@ -69,10 +69,11 @@ void launch_fill(const uint16_t *pool_dev, const CacheDesc *cache, const int32_t
 //
 // One persistent CTA per SM: warp 8 is the producer, warps 0..7 consume.  Work is a list of
 // tasks (work item u, block of R consecutive weight rows); the rows of a block are contiguous
-// in the entry, so the producer moves each block with one cp.async.bulk per matrix into a ring
-// of kStages shared-memory stages (mbarrier "full" with transaction bytes, "empty" with one
-// arrival per consumer warp).  Bytes in flight per SM are kStages stages, independent of
-// registers.  Consumers dot the rows with the item's token vectors from shared memory.
+// in the entry, so the producer moves each block with one cp.async.bulk per matrix into a
+// shared-memory stage (mbarrier "full" with transaction bytes, "empty" with the arrival of the
+// stage's one consumer warp; the stage-to-warp assignment is RingSmem::slot_of below).  Bytes
+// in flight per SM are the whole ring, independent of registers.  Consumers dot the rows with
+// the item's token vectors (from shared memory when they fit).
 // All waits are bounded; on a timeout the CTA records FT_ERR_TIMEOUT, waits (bounded) for its
 // own copies in flight and returns.
 // ---------------------------------------------------------------------------------------
@@ -231,12 +232,14 @@ __global__ void __launch_bounds__(kGemvThreads, 1) k_gateup_tma(
   const size_t x_bytes = XS ? (size_t)T * d * 2 : 0;
   RingSmem r = ring_layout(smem, x_bytes, stage_bytes, ring_bytes);
   const uint4 *xs = XS ? reinterpret_cast<const uint4 *>(smem) : reinterpret_cast<const uint4 *>(x);
+  ring_init(r);
+  // the work list, the fills and the slot table come from the kernels before; so may x (the
+  // previous call's output), which is staged only after the wait
+  pdl_wait();
   if (XS)
     for (int i = threadIdx.x; i < T * nchunk; i += blockDim.x)
       reinterpret_cast<uint4 *>(smem)[i] = __ldg(reinterpret_cast<const uint4 *>(x) + i);
-  ring_init(r);
   __syncthreads();
-  pdl_wait();  // the work list, the fills and the slot table come from the kernels before
   if (ctr->call_status != 0) return;
   const int n_work = ctr->n_work;
   const int n_jb = (d_ff + R - 1) / R;
@@ -463,18 +466,38 @@ __global__ void k_combine(const float *__restrict__ y, const float *__restrict__
   float acc[8];
 #pragma unroll
   for (int v = 0; v < 8; ++v) acc[v] = 0.f;
-  for (int j = 0; j < k; ++j) {
-    const float wj = w[t * k + j];
-    const float4 *row = reinterpret_cast<const float4 *>(y + (size_t)inv[t * k + j] * d) + 2 * c;
-    const float4 a = row[0], b = row[1];
-    acc[0] = fmaf(wj, a.x, acc[0]);
-    acc[1] = fmaf(wj, a.y, acc[1]);
-    acc[2] = fmaf(wj, a.z, acc[2]);
-    acc[3] = fmaf(wj, a.w, acc[3]);
-    acc[4] = fmaf(wj, b.x, acc[4]);
-    acc[5] = fmaf(wj, b.y, acc[5]);
-    acc[6] = fmaf(wj, b.z, acc[6]);
-    acc[7] = fmaf(wj, b.w, acc[7]);
+  // groups of 8 ranks: all row addresses, then all row loads, then the sums in rank order
+  for (int j0 = 0; j0 < k; j0 += 8) {
+    const int nj = min(8, k - j0);
+    float wj[8];
+    int rj[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      wj[u] = u < nj ? w[t * k + j0 + u] : 0.f;
+      rj[u] = u < nj ? inv[t * k + j0 + u] : 0;
+    }
+    float4 ra[8], rb[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      if (u < nj) {
+        const float4 *row = reinterpret_cast<const float4 *>(y + (size_t)rj[u] * d) + 2 * c;
+        ra[u] = row[0];
+        rb[u] = row[1];
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      if (u < nj) {
+        acc[0] = fmaf(wj[u], ra[u].x, acc[0]);
+        acc[1] = fmaf(wj[u], ra[u].y, acc[1]);
+        acc[2] = fmaf(wj[u], ra[u].z, acc[2]);
+        acc[3] = fmaf(wj[u], ra[u].w, acc[3]);
+        acc[4] = fmaf(wj[u], rb[u].x, acc[4]);
+        acc[5] = fmaf(wj[u], rb[u].y, acc[5]);
+        acc[6] = fmaf(wj[u], rb[u].z, acc[6]);
+        acc[7] = fmaf(wj[u], rb[u].w, acc[7]);
+      }
+    }
   }
   if (shared) {
     const float4 *row = reinterpret_cast<const float4 *>(y + (size_t)(T * k + t) * d) + 2 * c;
@@ -512,7 +535,7 @@ void launch_down_gemv(const WorkItem *work, DevCounters *ctr, int max_work, cons
 void launch_combine(const float *y, const float *w, const int32_t *inv, const DevCounters *ctr,
                     uint16_t *out, int T, int k, int d, int shared, cudaStream_t s) {
   const int n = T * (d >> 3);
-  launch_pdl(k_combine, dim3((n + 255) / 256), dim3(256), 0, s, y, w, inv, ctr, out, T, k, d,
+  launch_pdl(k_combine, dim3((n + 127) / 128), dim3(128), 0, s, y, w, inv, ctr, out, T, k, d,
              shared);
 }
 

@@ -98,6 +98,9 @@ struct ft_moe {
   cudaStream_t copy_stream = nullptr;
   std::vector<cudaEvent_t> ev_cs, ev_ce, ev_ks, ev_ke;  // copy start/end, compute start/end
   int last_prefill_layers = 0;
+  int prefill_topup = 0;
+  uint64_t last_h2d_bytes = 0, last_d2d_bytes = 0;  // moved by the last prefill
+  std::vector<int32_t> table_host;                  // slot table read by the top-up
 
   // host staging for decode_host
   uint16_t *xstage = nullptr, *ostage = nullptr;
@@ -354,7 +357,7 @@ int ft_moe_create(int L, int E, int k, int d, int d_ff, int n_slots, const ft_mo
                 "need d in [128, 4096] and d_ff in [128, 8192], multiples of 128 (got %d, %d)", d,
                 d_ff);
   if (n_slots < 1) return fail(FT_ERR_INVALID, "n_slots must be >= 1 (got %d)", n_slots);
-  ft_moe_opts o{0, 1, 4096, 0};
+  ft_moe_opts o{0, 1, 4096, 0, 0};
   if (opts) o = *opts;
   if (o.max_tokens < 1 || o.max_tokens > (1 << 20))
     return fail(FT_ERR_INVALID, "max_tokens out of range (%d)", o.max_tokens);
@@ -371,6 +374,7 @@ int ft_moe_create(int L, int E, int k, int d, int d_ff, int n_slots, const ft_mo
   h->n_shared = o.n_shared;
   h->prewarm = o.prewarm;
   h->debug = o.debug_checks;
+  h->prefill_topup = o.prefill_topup != 0;
   h->entry_elems = (size_t)3 * d * d_ff;
   h->entry_bytes = h->entry_elems * 2;
   h->has_bias.assign(L, 0);
@@ -655,11 +659,45 @@ int ft_moe_prefill_stream(ft_moe *h, int layer0, int n_layers, const void *x, in
   cudaEvent_t start = h->ev_ks[0];
   FT_CUDA(cudaEventRecord(start, s));
   FT_CUDA(cudaStreamWaitEvent(h->copy_stream, start, 0));
+  // top-up: the slot table as of everything already queued on `stream`
+  if (h->prefill_topup) {
+    FT_CUDA(cudaStreamSynchronize(s));
+    h->table_host.resize((size_t)h->L * h->E);
+    FT_CUDA(cudaMemcpy(h->table_host.data(), h->slot_table, h->table_host.size() * sizeof(int32_t),
+                       cudaMemcpyDeviceToHost));
+  }
+  h->last_h2d_bytes = h->last_d2d_bytes = 0;
+  const size_t eb = h->entry_bytes;
   auto enqueue_copy = [&](int i) -> int {
+    const int l = layer0 + i;
+    uint8_t *dst = reinterpret_cast<uint8_t *>(h->dbuf[i & 1]);
+    const uint8_t *src = pool + (size_t)l * layer_bytes;
     if (i >= 2) FT_CUDA(cudaStreamWaitEvent(h->copy_stream, h->ev_ke[i - 2], 0));
     FT_CUDA(cudaEventRecord(h->ev_cs[i], h->copy_stream));
-    FT_CUDA(cudaMemcpyAsync(h->dbuf[i & 1], pool + (size_t)(layer0 + i) * layer_bytes, layer_bytes,
-                            cudaMemcpyHostToDevice, h->copy_stream));
+    if (!h->prefill_topup) {
+      FT_CUDA(cudaMemcpyAsync(dst, src, layer_bytes, cudaMemcpyHostToDevice, h->copy_stream));
+      h->last_h2d_bytes += layer_bytes;
+    } else {
+      const int32_t *row = h->table_host.data() + (size_t)l * h->E;
+      const uint8_t *slots = reinterpret_cast<const uint8_t *>(h->slots);
+      for (int e = 0; e < h->E;) {
+        const int sl = row[e];
+        if (sl >= 0) {  // resident: slot -> buffer
+          FT_CUDA(cudaMemcpyAsync(dst + (size_t)e * eb, slots + (size_t)sl * eb, eb,
+                                  cudaMemcpyDeviceToDevice, h->copy_stream));
+          h->last_d2d_bytes += eb;
+          ++e;
+        } else {        // a maximal run of absent experts: one host -> device copy
+          int e1 = e + 1;
+          while (e1 < h->E && row[e1] < 0) ++e1;
+          const size_t n = (size_t)(e1 - e) * eb;
+          FT_CUDA(cudaMemcpyAsync(dst + (size_t)e * eb, src + (size_t)e * eb, n,
+                                  cudaMemcpyHostToDevice, h->copy_stream));
+          h->last_h2d_bytes += n;
+          e = e1;
+        }
+      }
+    }
     FT_CUDA(cudaEventRecord(h->ev_ce[i], h->copy_stream));
     return FT_OK;
   };
@@ -678,6 +716,14 @@ int ft_moe_prefill_stream(ft_moe *h, int layer0, int n_layers, const void *x, in
   h->last_stream = s;
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return fail(FT_ERR_CUDA, "prefill launch: %s", cudaGetErrorString(e));
+  return FT_OK;
+}
+
+int ft_moe_prefill_bytes(ft_moe *h, uint64_t *h2d_bytes, uint64_t *d2d_bytes) {
+  if (int r = check_handle(h)) return r;
+  if (h->last_prefill_layers == 0) return fail(FT_ERR_STATE, "no prefill has run");
+  if (h2d_bytes) *h2d_bytes = h->last_h2d_bytes;
+  if (d2d_bytes) *d2d_bytes = h->last_d2d_bytes;
   return FT_OK;
 }
 

@@ -326,7 +326,9 @@ void launch_perm_multi(const ControlArgs &a, int32_t *chunk_scratch, cudaStream_
 
 // ---------------------------------------------------------------------------------------
 // Control: one CTA of 1024 threads.
-//   1. (unless perm_ready) counts, offsets and the stable grouping of the P pairs;
+//   1. counts, offsets and the stable grouping of the P = T*k pairs by expert (from the
+//      pairs the in-CTA top-k left in shared memory, from idx in global memory, or, when
+//      perm_ready, as a multi-CTA pass left them);
 //   2. decode: the LRU update.  Touched set S = experts with count > 0.  Hits (ascending e)
 //      get stamps tick0+1.., misses (ascending e) take the lowest free slots, then the
 //      eligible slots (stamp <= tick0) in increasing (stamp, slot) order, and get stamps
@@ -334,44 +336,293 @@ void launch_perm_multi(const ControlArgs &a, int32_t *chunk_scratch, cudaStream_
 //      FT_ERR_CAPACITY and leaves the cache and the outputs untouched.
 //      prefill: expert e reads entry e of the layer's double buffer.
 //   3. the work list (touched experts ascending, then the shared expert) and counters.
+// Threads leave data-dependent loops at different times; every block barrier that may
+// follow such a loop is preceded by __syncwarp() (cta_sync), so warps reach it converged.
 // ---------------------------------------------------------------------------------------
-constexpr int kStampSmem = 2048;  // slots whose eviction keys are staged in shared memory
+constexpr int kStampSmem = 2048;                     // slots whose keys fit in shared memory
+constexpr int kTopkSmem = 4096;                      // T*E logits for the in-CTA top-k
+constexpr int kPairSmem = kGemvMaxTokens * kMaxK;    // pairs of the in-CTA top-k
+constexpr int kFieldBits = 21;                       // packed per-expert scan fields
+constexpr unsigned long long kFieldMask = (1ull << kFieldBits) - 1;
 
-__device__ __forceinline__ void control_body(const ControlArgs &a, int perm_ready) {
-  __shared__ int s_cnt[kMaxE];
-  __shared__ int s_off[kMaxE + 1];
-  __shared__ int s_base[kMaxE];
-  __shared__ int s_list[kMaxE];    // free slots, in increasing slot order
-  __shared__ int s_victim[kMaxE];  // victims, in increasing (stamp, slot) order
-  __shared__ int s_warp[32];
-  __shared__ unsigned long long s_key[kStampSmem];
+enum { kMiscNear = 0, kMiscDigit, kMiscNeed, kMiscCand, kMiscErr, kMiscN };
+
+struct CtlSmem {
+  int cnt[kMaxE];
+  int off[kMaxE + 1];
+  int slot[kMaxE];  // grouping: running base per expert; LRU: slot taken by miss rank m
+  int cand[kMaxE];  // eviction candidates below the threshold key
+  int hist[2][256];
+  unsigned long long wsum[32];
+  int misc[kMiscN];
+  int pe[kPairSmem];    // expert of pair p (in-CTA top-k)
+  float pv[kPairSmem];  // its logit
+  float next[kGemvMaxTokens];  // (k+1)-th logit of token t
+  union {
+    float logit[kTopkSmem];
+    unsigned long long key[kStampSmem];
+  } u;
+};
+
+__device__ __forceinline__ void cta_sync() {
+  __syncwarp();
+  __syncthreads();
+}
+
+// Inclusive scan over the 1024 threads of the CTA; *total = sum over all threads.
+__device__ __forceinline__ unsigned long long cta_scan_u64(unsigned long long v,
+                                                           unsigned long long *wsum,
+                                                           unsigned long long *total) {
+  __syncwarp();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const unsigned long long o = __shfl_up_sync(0xffffffffu, v, off);
+    if (lane >= off) v += o;
+  }
+  if (lane == 31) wsum[warp] = v;
+  cta_sync();
+  if (warp == 0) {
+    unsigned long long wv = wsum[lane];
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const unsigned long long o = __shfl_up_sync(0xffffffffu, wv, off);
+      if (lane >= off) wv += o;
+    }
+    wsum[lane] = wv;
+  }
+  cta_sync();
+  if (warp > 0) v += wsum[warp - 1];
+  *total = wsum[31];
+  cta_sync();
+  return v;
+}
+
+// Top-k of T tokens inside the CTA (T*E <= kTopkSmem, T <= kGemvMaxTokens): every (t, e)
+// counts the experts that beat it under (logit descending, id ascending); rank r < k puts
+// e at position r.  Gates w_j = exp(l_j - l_0) / sum_i exp(l_i - l_0); near-tie when two
+// adjacent selected logits, or the k-th and (k+1)-th, differ by <= kNearTie (in double).
+// Leaves pair p = t*k + j in sm.pe / sm.pv and returns thread p's gate.
+__device__ __forceinline__ float topk_cta(const ControlArgs &a, const float *logits,
+                                          CtlSmem &sm) {
+  const int T = a.T, E = a.E, k = a.k, n = T * E, tid = threadIdx.x;
+  for (int i = tid; i < n; i += 1024) sm.u.logit[i] = __ldcg(logits + i);
+  cta_sync();
+  for (int i = tid; i < n; i += 1024) {
+    const int t = i / E, e = i - t * E;
+    const float v = sm.u.logit[i];
+    const float *row = sm.u.logit + t * E;
+    int rank = 0;
+    for (int e2 = 0; e2 < E && rank <= k; ++e2) {
+      const float v2 = row[e2];
+      rank += (v2 > v || (v2 == v && e2 < e)) ? 1 : 0;
+    }
+    if (rank < k) {
+      sm.pe[t * k + rank] = e;
+      sm.pv[t * k + rank] = v;
+    } else if (rank == k) {
+      sm.next[t] = v;
+    }
+  }
+  cta_sync();
+  float w = 0.f;
+  if (tid < T * k) {
+    const int t = tid / k, j = tid - t * k;
+    const float *pv = sm.pv + t * k;
+    const float l0 = pv[0];
+    float sum = 0.f;
+    for (int i = 0; i < k; ++i) sum += expf(pv[i] - l0);
+    w = expf(pv[j] - l0) / sum;
+    const_cast<int32_t *>(a.idx)[tid] = sm.pe[tid];
+    const_cast<float *>(a.w)[tid] = w;
+    if (j == 0) {
+      bool near = false;
+      for (int i = 0; i + 1 < k; ++i) near = near || ((double)pv[i] - (double)pv[i + 1]) <= kNearTie;
+      if (k < E) near = near || ((double)pv[k - 1] - (double)sm.next[t]) <= kNearTie;
+      const_cast<uint8_t *>(a.tie)[t] = near ? 1 : 0;
+      if (near) atomicAdd(&sm.misc[kMiscNear], 1);
+    }
+  }
+  return w;
+}
+
+// The nv smallest eviction keys (stamp of an occupied slot with stamp <= tick0; others are
+// not eligible) in increasing (stamp, slot) order -> out[0 .. nv).  A radix select (8-bit
+// digits from the top bit of tick0) finds the nv-th smallest stamp v*; the slots with a
+// smaller stamp are ranked among themselves, the ones at v* follow in slot order.
+// Returns false (and writes nothing) if fewer than nv slots are eligible.
+__device__ bool select_victims(const CacheDesc &cd, unsigned long long tick0, int nv, int *out,
+                               CtlSmem &sm) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int n = cd.n_slots;
+  const bool in_smem = n <= kStampSmem;
+  auto key_g = [&](int s) -> unsigned long long {
+    const unsigned long long st = cd.stamps[s];
+    return (cd.owner[s] >= 0 && st <= tick0) ? st : ~0ull;
+  };
+  auto key = [&](int s) -> unsigned long long { return in_smem ? sm.u.key[s] : key_g(s); };
+  if (in_smem)
+    for (int s = tid; s < n; s += 1024) sm.u.key[s] = key_g(s);
+  for (int i = tid; i < 512; i += 1024) (&sm.hist[0][0])[i] = 0;
+  if (tid == 0) {
+    sm.misc[kMiscErr] = 0;
+    sm.misc[kMiscCand] = 0;
+  }
+  cta_sync();
+  const int nbits = 64 - __clzll(tick0 | 1ull);
+  unsigned long long prefix = 0;  // digits of v* fixed so far
+  int need = nv;                  // rank of v* among the keys that match the prefix
+  int buf = 0;
+  for (int shift = ((nbits + 7) / 8 - 1) * 8; shift >= 0; shift -= 8, buf ^= 1) {
+    int *hist = sm.hist[buf];
+    for (int s = tid; s < n; s += 1024) {
+      const unsigned long long kk = key(s);
+      if (kk != ~0ull && ((kk >> shift) >> 8) == prefix) atomicAdd(&hist[(kk >> shift) & 255], 1);
+    }
+    cta_sync();
+    if (warp == 0) {
+      int c[8], local = 0;
+#pragma unroll
+      for (int b = 0; b < 8; ++b) {
+        c[b] = hist[8 * lane + b];
+        local += c[b];
+      }
+      int incl = local;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int o = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += o;
+      }
+      const int excl = incl - local;
+      if (excl < need && need <= incl) {
+        int cum = excl;
+#pragma unroll
+        for (int b = 0; b < 8; ++b) {
+          if (cum < need && need <= cum + c[b]) {
+            sm.misc[kMiscDigit] = 8 * lane + b;
+            sm.misc[kMiscNeed] = need - cum;
+          }
+          cum += c[b];
+        }
+      }
+      if (lane == 31 && incl < need) sm.misc[kMiscErr] = 1;
+      for (int b = lane; b < 256; b += 32) sm.hist[buf ^ 1][b] = 0;
+    }
+    cta_sync();
+    if (sm.misc[kMiscErr]) return false;
+    prefix = (prefix << 8) | (unsigned long long)sm.misc[kMiscDigit];
+    need = sm.misc[kMiscNeed];
+  }
+  const unsigned long long vstar = prefix;
+  // keys below v*: exactly nv - need of them
+  for (int s = tid; s < n; s += 1024)
+    if (key(s) < vstar) sm.cand[atomicAdd(&sm.misc[kMiscCand], 1)] = s;
+  cta_sync();
+  const int na = sm.misc[kMiscCand];
+  for (int i = tid; i < na; i += 1024) {
+    const int s = sm.cand[i];
+    const unsigned long long kk = key(s);
+    int r = 0;
+    for (int i2 = 0; i2 < na; ++i2) {
+      const int s2 = sm.cand[i2];
+      const unsigned long long k2 = key(s2);
+      r += (k2 < kk || (k2 == kk && s2 < s)) ? 1 : 0;
+    }
+    out[r] = s;
+  }
+  // keys equal to v*: the `need` lowest slot ids
+  int base = 0;
+  for (int c0 = 0; c0 < n && base < need; c0 += 1024) {
+    const int s = c0 + tid;
+    const bool f = s < n && key(s) == vstar;
+    unsigned long long tot;
+    const int r = (int)cta_scan_u64(f ? 1ull : 0ull, sm.wsum, &tot) - (f ? 1 : 0);
+    if (f && base + r < need) out[na + base + r] = s;
+    base += (int)tot;
+  }
+  cta_sync();
+  return true;
+}
+
+// mode: 0 = pairs from idx in global memory (P <= kPermSingleMax), 1 = perm_ready (counts
+// and offsets from a multi-CTA pass), 2 = in-CTA top-k from `logits` (fused decode).
+__device__ __forceinline__ void control_body(const ControlArgs &a, int mode,
+                                             const float *logits) {
+  __shared__ CtlSmem sm;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int E = a.E, P = a.P;
-  int total;
+  const bool lru = a.slot_table != nullptr;
+  int *table = lru ? a.slot_table + (size_t)a.layer * E : nullptr;
+  const int cur = (lru && tid < E) ? table[tid] : -1;  // issued early, used after grouping
   if (tid == 0) a.ctr->call_status = 0;
+  if (tid < kMiscN) sm.misc[tid] = 0;
+  for (int e = tid; e < E; e += 1024) sm.cnt[e] = 0;
+  cta_sync();
 
-  if (!perm_ready) {
-    for (int e = tid; e < E; e += 1024) s_cnt[e] = 0;
-    __syncthreads();
+  // 1. counts (and, below, offsets and grouping)
+  float my_w = 0.f;
+  if (mode == 2) {
+    my_w = topk_cta(a, logits, sm);
+    if (tid < P) atomicAdd(&sm.cnt[sm.pe[tid]], 1);
+  } else if (mode == 0) {
     for (int p = tid; p < P; p += 1024) {
       const int e = a.idx[p];
       if (e >= 0 && e < E)
-        atomicAdd(&s_cnt[e], 1);
+        atomicAdd(&sm.cnt[e], 1);
       else
         set_status(a.ctr, FT_ERR_INVALID);
     }
-    __syncthreads();
-    {
-      const int v = (tid < E) ? s_cnt[tid] : 0;
-      const int incl = block_incl_scan(v, s_warp, &total);
-      if (tid < E) {
-        s_off[tid] = incl - v;
-        s_base[tid] = incl - v;
-      }
-      if (tid == 0) s_off[E] = P;
+  } else {
+    for (int e = tid; e < E; e += 1024) sm.cnt[e] = a.counts[e];
+  }
+  cta_sync();
+
+  // one scan over experts: offsets (modes 0, 2), hit / touched rank, miss rank
+  const int cnt = tid < E ? sm.cnt[tid] : 0;
+  const bool touched = cnt > 0;
+  const bool hit = lru ? (touched && cur >= 0) : touched;
+  const bool miss = lru && touched && cur < 0;
+  const unsigned long long pk = (mode == 1 ? 0ull : (unsigned long long)cnt) |
+                                ((unsigned long long)hit << kFieldBits) |
+                                ((unsigned long long)miss << (2 * kFieldBits));
+  unsigned long long tot;
+  const unsigned long long ex = cta_scan_u64(pk, sm.wsum, &tot) - pk;
+  const int hrank = (int)((ex >> kFieldBits) & kFieldMask);
+  const int mrank = (int)(ex >> (2 * kFieldBits));
+  const int n_hit = (int)((tot >> kFieldBits) & kFieldMask);
+  const int n_miss = (int)(tot >> (2 * kFieldBits));
+  const int n_touched = n_hit + n_miss;
+  const int trank = hrank + mrank;
+  if (mode == 1) {
+    for (int e = tid; e <= E; e += 1024) sm.off[e] = a.offsets[e];
+  } else {
+    if (tid < E) {
+      sm.off[tid] = (int)(ex & kFieldMask);
+      sm.slot[tid] = (int)(ex & kFieldMask);
+      a.counts[tid] = cnt;
+      a.offsets[tid] = (int)(ex & kFieldMask);
     }
-    __syncthreads();
-    // stable scatter: chunks of 1024 pairs, the warps of a chunk in order
+    if (tid == 0) {
+      sm.off[E] = P;
+      a.offsets[E] = P;
+    }
+  }
+  cta_sync();
+
+  // grouping: pair p goes to off[e] + #{p' < p with the same expert}
+  if (mode == 2) {
+    if (tid < P) {
+      const int e = sm.pe[tid];
+      int r = 0;
+      for (int p2 = 0; p2 < tid; ++p2) r += (sm.pe[p2] == e) ? 1 : 0;
+      const int pos = sm.off[e] + r;
+      a.perm[pos] = tid;
+      a.inv[tid] = pos;
+      a.tok[pos] = tid / a.k;
+      a.wq[pos] = my_w;
+    }
+  } else if (mode == 0) {
+    // chunks of 1024 pairs; inside a chunk the warps go in order
     for (int pc = 0; pc < P; pc += 1024) {
       const int p = pc + tid;
       int e = (p < P) ? a.idx[p] : -1;
@@ -386,49 +637,39 @@ __device__ __forceinline__ void control_body(const ControlArgs &a, int perm_read
       const int nwarps = min(32, (P - pc + 31) / 32);
       for (int w2 = 0; w2 < nwarps; ++w2) {
         if (warp == w2 && e >= 0) {
-          const int pos = s_base[e] + rank;
+          const int pos = sm.slot[e] + rank;
           a.perm[pos] = p;
           a.inv[p] = pos;
           a.tok[pos] = p / a.k;
           a.wq[pos] = a.w[p];
         }
         __syncwarp();
-        if (warp == w2 && e >= 0 && rank == 0) s_base[e] += __popc(mask);
-        __syncthreads();
+        if (warp == w2 && e >= 0 && rank == 0) sm.slot[e] += __popc(mask);
+        cta_sync();
       }
     }
-    for (int e = tid; e < E; e += 1024) a.counts[e] = s_cnt[e];
-    for (int e = tid; e <= E; e += 1024) a.offsets[e] = s_off[e];
-  } else {
-    for (int e = tid; e < E; e += 1024) s_cnt[e] = a.counts[e];
-    for (int e = tid; e <= E; e += 1024) s_off[e] = a.offsets[e];
   }
-  __syncthreads();
   if (a.shared) {
     for (int t = tid; t < a.T; t += 1024) {
       a.tok[P + t] = t;
       a.wq[P + t] = 1.0f;
     }
   }
-
-  // touched experts, ranked in ascending id
-  const bool touched = tid < E && s_cnt[tid] > 0;
-  const int trank = block_incl_scan(touched ? 1 : 0, s_warp, &total) - (touched ? 1 : 0);
-  const int n_touched = total;
-
   // near-tie count of this call
-  if (warp == 0) {
+  if (mode != 2 && warp == 0) {
     int nt = 0;
     for (int t = lane; t < a.T; t += 32) nt += a.tie[t] ? 1 : 0;
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) nt += __shfl_xor_sync(0xffffffffu, nt, off);
-    if (lane == 0 && nt) atomicAdd(&a.ctr->near_ties, (unsigned long long)nt);
+    if (lane == 0) sm.misc[kMiscNear] = nt;
   }
 
+  // 2. the LRU update
   int slot_of = -1;
   CacheDesc cd{};
-  if (a.slot_table) cd = *a.cache;
-  if (a.slot_table) {
+  int nv = 0;
+  if (lru) {
+    cd = *a.cache;
     if (n_touched > cd.n_slots) {
       if (tid == 0) {
         set_status(a.ctr, FT_ERR_CAPACITY);
@@ -439,59 +680,42 @@ __device__ __forceinline__ void control_body(const ControlArgs &a, int perm_read
       return;
     }
     const unsigned long long tick0 = a.ctr->tick;
-    int *table = a.slot_table + (size_t)a.layer * E;
-    const int cur = touched ? table[tid] : -1;
-    const bool hit = touched && cur >= 0;
-    const bool miss = touched && cur < 0;
-    const int hrank = block_incl_scan(hit ? 1 : 0, s_warp, &total) - (hit ? 1 : 0);
-    const int n_hit = total;
-    const int mrank = block_incl_scan(miss ? 1 : 0, s_warp, &total) - (miss ? 1 : 0);
-    const int n_miss = total;
     if (hit) {
       if (cur < cd.n_slots)
         cd.stamps[cur] = tick0 + 1 + (unsigned long long)hrank;
       else
         set_status(a.ctr, FT_ERR_INVALID);
     }
-    // the n_miss lowest free slots
     int n_free = 0;
-    for (int base = 0; base < cd.n_slots; base += 1024) {
-      const int s = base + tid;
-      const bool f = s < cd.n_slots && cd.owner[s] < 0;
-      const int r = block_incl_scan(f ? 1 : 0, s_warp, &total) - (f ? 1 : 0);
-      if (f && n_free + r < n_miss) s_list[n_free + r] = s;
-      n_free += total;
-      if (n_free >= n_miss) break;
-    }
-    const int nv = n_miss > n_free ? n_miss - n_free : 0;
-    if (nv > 0) {
-      // eviction keys: (stamp, slot) of occupied slots not touched in this call
-      const bool in_smem = cd.n_slots <= kStampSmem;
-      if (in_smem) {
-        for (int s = tid; s < cd.n_slots; s += 1024) {
-          const unsigned long long st = cd.stamps[s];
-          s_key[s] = (cd.owner[s] >= 0 && st <= tick0) ? st : ~0ull;
+    if (n_miss > 0) {
+      cta_sync();  // hit stamps written before eviction keys are read
+      // the n_miss lowest free slots (none to look for once every slot is occupied)
+      if (a.ctr->occupied < cd.n_slots) {
+        for (int b0 = 0; b0 < cd.n_slots && n_free < n_miss; b0 += 1024) {
+          const int s = b0 + tid;
+          const bool f = s < cd.n_slots && cd.owner[s] < 0;
+          unsigned long long tf;
+          const int r = (int)cta_scan_u64(f ? 1ull : 0ull, sm.wsum, &tf) - (f ? 1 : 0);
+          if (f && n_free + r < n_miss) sm.slot[n_free + r] = s;
+          n_free += (int)tf;
         }
+        n_free = min(n_free, n_miss);
       }
-      __syncthreads();
-      for (int s = tid; s < cd.n_slots; s += 1024) {
-        const unsigned long long ks =
-            in_smem ? s_key[s] : ((cd.owner[s] >= 0 && cd.stamps[s] <= tick0) ? cd.stamps[s] : ~0ull);
-        if (ks == ~0ull) continue;
-        int rank = 0;
-        for (int s2 = 0; s2 < cd.n_slots && rank < nv; ++s2) {
-          const unsigned long long k2 =
-              in_smem ? s_key[s2]
-                      : ((cd.owner[s2] >= 0 && cd.stamps[s2] <= tick0) ? cd.stamps[s2] : ~0ull);
-          rank += (k2 < ks || (k2 == ks && s2 < s)) ? 1 : 0;
+      nv = n_miss - n_free;
+      if (nv > 0 && !select_victims(cd, tick0, nv, sm.slot + n_free, sm)) {
+        if (tid == 0) {
+          set_status(a.ctr, FT_ERR_INVALID);
+          a.ctr->call_status = FT_ERR_INVALID;
+          a.ctr->n_work = 0;
+          a.ctr->n_fill = 0;
         }
-        if (rank < nv) s_victim[rank] = s;
+        return;
       }
+      cta_sync();
     }
-    __syncthreads();
     if (miss) {
       const int m = mrank;
-      const int slot = (m < n_free) ? s_list[m] : s_victim[m - n_free];
+      const int slot = sm.slot[m];
       if (m >= n_free) {
         const int ev = cd.owner[slot];
         if (ev >= 0 && ev < a.L * E) a.slot_table[ev] = -1;
@@ -520,15 +744,18 @@ __device__ __forceinline__ void control_body(const ControlArgs &a, int perm_read
     slot_of = touched ? tid : -1;
     if (tid == 0) a.ctr->n_fill = 0;
   }
+
+  // 3. work list and counters
   if (touched) {
     WorkItem wi;
-    wi.W = (a.slot_table ? cd.slots : a.buffer) + (size_t)slot_of * a.entry_elems;
-    wi.q0 = s_off[tid];
-    wi.count = s_cnt[tid];
+    wi.W = (lru ? cd.slots : a.buffer) + (size_t)slot_of * a.entry_elems;
+    wi.q0 = sm.off[tid];
+    wi.count = cnt;
     wi.expert = tid;
     wi.slot = slot_of;
     a.work[trank] = wi;
   }
+  cta_sync();
   if (tid == 0) {
     int nw = n_touched;
     if (a.shared) {
@@ -541,17 +768,19 @@ __device__ __forceinline__ void control_body(const ControlArgs &a, int perm_read
       a.work[nw++] = wi;
     }
     a.ctr->n_work = nw;
+    if (sm.misc[kMiscNear]) atomicAdd(&a.ctr->near_ties, (unsigned long long)sm.misc[kMiscNear]);
   }
 }
 
 __global__ void __launch_bounds__(1024) k_control(ControlArgs a, int perm_ready) {
-  control_body(a, perm_ready);
+  control_body(a, perm_ready ? 1 : 0, nullptr);
 }
 
 // ---------------------------------------------------------------------------------------
 // Decode routing in one launch (T <= kGemvMaxTokens): every CTA computes a block of router
 // logits; the CTA that finishes last (atomic arrival counter, no waiting) runs the top-k of
-// all T tokens, one warp per token, and then the control body above.
+// all T tokens and then the control body above.  With T*E <= kTopkSmem the top-k runs on
+// the whole CTA from shared memory; otherwise one warp per token.
 // ---------------------------------------------------------------------------------------
 template <int TT, int EE, int NV>
 __global__ void __launch_bounds__(1024) k_route_decode(const uint16_t *__restrict__ x,
@@ -565,16 +794,30 @@ __global__ void __launch_bounds__(1024) k_route_decode(const uint16_t *__restric
   const int n_eb = (E + EE - 1) / EE;
   const int n_tasks = ((T + TT - 1) / TT) * n_eb;
   const int task = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+  // The router weights change only through ft_moe_load_router (a copy, fully ordered):
+  // stage this warp's rows in L2 while the previous kernel finishes.  x may be that
+  // kernel's output and the bias a copy queued after it, so both are read after the wait.
+  if (task < n_tasks) {
+    const int e0 = (task % n_eb) * EE, nchunk = a.d >> 3;
+    for (int c = lane; c < nchunk; c += 32)
+#pragma unroll
+      for (int j = 0; j < EE; ++j)
+        if (e0 + j < E) prefetch_l2(wr + (size_t)(e0 + j) * a.d + (size_t)c * 8);
+  }
+  pdl_wait();
   if (task < n_tasks) {
     const int tb = task / n_eb, eb = task - tb * n_eb;
     const int t0 = tb * TT, e0 = eb * EE;
+    float bv[EE];
+#pragma unroll
+    for (int j = 0; j < EE; ++j) bv[j] = (bias && e0 + j < E) ? __ldg(bias + e0 + j) : 0.f;
     float acc[TT][EE];
 #pragma unroll
     for (int i = 0; i < TT; ++i)
 #pragma unroll
       for (int j = 0; j < EE; ++j) acc[i][j] = 0.f;
     const int d = a.d, nchunk = d >> 3;
-#pragma unroll 2
+#pragma unroll(TT * EE <= 2 ? 4 : 2)
     for (int c = lane; c < nchunk; c += 32) {
       uint4 xv[TT], wv[EE];
 #pragma unroll
@@ -603,17 +846,15 @@ __global__ void __launch_bounds__(1024) k_route_decode(const uint16_t *__restric
       for (int j = 0; j < EE; ++j) {
         if (lane == ((i * EE + j) & 31) && t0 + i < T && e0 + j < E) {
           float v = acc[i][j];
-          if (bias) v = v + bias[e0 + j];
+          if (bias) v = v + bv[j];
           logits[(size_t)(t0 + i) * E + e0 + j] = v;
         }
       }
   }
-  // the previous kernel (which reads the routing state this launch rewrites) must be done
-  pdl_wait();
   // the last CTA to arrive continues
   __shared__ int s_last;
   __threadfence();
-  __syncthreads();
+  cta_sync();
   if (threadIdx.x == 0) {
     const unsigned prev = atomicAdd(&a.ctr->route_arrive, 1u);
     s_last = (prev == gridDim.x - 1) ? 1 : 0;
@@ -621,13 +862,17 @@ __global__ void __launch_bounds__(1024) k_route_decode(const uint16_t *__restric
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  const int warp = threadIdx.x >> 5;
-  for (int t = warp; t < T; t += 32)
-    topk_warp<NV>(logits + (size_t)t * E, E, a.k, const_cast<int32_t *>(a.idx) + (size_t)t * a.k,
-                  const_cast<float *>(a.w) + (size_t)t * a.k, const_cast<uint8_t *>(a.tie) + t);
-  __syncthreads();
   if (threadIdx.x == 0) a.ctr->route_arrive = 0;
-  control_body(a, 0);
+  if (T * E <= kTopkSmem) {
+    control_body(a, 2, logits);
+  } else {
+    const int warp = threadIdx.x >> 5;
+    for (int t = warp; t < T; t += 32)
+      topk_warp<NV>(logits + (size_t)t * E, E, a.k, const_cast<int32_t *>(a.idx) + (size_t)t * a.k,
+                    const_cast<float *>(a.w) + (size_t)t * a.k, const_cast<uint8_t *>(a.tie) + t);
+    cta_sync();
+    control_body(a, 0, nullptr);
+  }
 }
 
 void launch_route_decode(const uint16_t *x, const uint16_t *wr, const float *bias, float *logits,

@@ -65,6 +65,8 @@ typedef struct {
                            lexicographic order, slots 0..min(n_slots,L*E)-1, stamps 1..n  */
   int max_tokens;   /* [4096] largest T accepted by forward / prefill (sizes scratch)     */
   int debug_checks; /* [0] kernels re-check slot indices and record violations           */
+  int prefill_topup; /* [0] 1 = prefill copies entries already resident in cache slots
+                            device -> device and streams only the rest from the host      */
 } ft_moe_opts;
 
 /* Cache counters, accumulated on the device since creation or the last reset. */
@@ -155,7 +157,8 @@ int ft_moe_decode_host(ft_moe *h, int layer0, int n_layers, const void *x_host, 
 /*
  * Prefill with full-layer double buffering: for i = 0 .. n_layers-1, computes
  * out[i] = MoE layer (layer0+i) applied to x (device bf16 [T][d]); out is device bf16
- * [n_layers][T][d].  All E experts of layer l+1 are copied host -> device into the back
+ * [n_layers][T][d].  All E experts of layer l+1 are copied into the back buffer (host ->
+ * device, or from cache slots with the top-up option below)
  * buffer on an internal copy stream while layer l computes on `stream`.  Prefill reads
  * the double buffer only: it neither reads nor updates the LRU cache.  Allocates the
  * 2 x E-entry double buffer on first use.  Returns after enqueueing; `stream` waits for
@@ -163,6 +166,21 @@ int ft_moe_decode_host(ft_moe *h, int layer0, int n_layers, const void *x_host, 
  */
 int ft_moe_prefill_stream(ft_moe *h, int layer0, int n_layers, const void *x, int T, void *out,
                           ft_stream_t stream);
+/*
+ * Prefill top-up (opts.prefill_topup = 1), an extension beyond the pages: FreeToken's
+ * full-layer streaming ("Prefill double-buffering") copies every expert of a layer over the
+ * host link even when the decode cache ("FreeToken pages" LRU) already holds some of them.
+ * With the option set, ft_moe_prefill_stream synchronises `stream` once, reads the slot
+ * table, and fills each layer's back buffer with a device -> device copy from the slot of
+ * every resident (layer, expert) and host -> device copies of the maximal runs of absent
+ * experts.  The buffer contents, and so the results, are the same as without the option;
+ * the LRU stays untouched (no stamps, no counters).  Forward calls on other streams must
+ * not be in flight during the prefill (the handle is single-stream, as everywhere).
+ */
+
+/* Bytes the most recent prefill moved into the double buffer: host -> device and
+ * slot -> buffer (device -> device).  Either pointer may be NULL. */
+int ft_moe_prefill_bytes(ft_moe *h, uint64_t *h2d_bytes, uint64_t *d2d_bytes);
 
 /* Timing of the most recent prefill (milliseconds, from CUDA events): per-layer copy and
  * compute spans, summed, and the wall time from first copy to last compute. */

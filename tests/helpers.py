@@ -46,12 +46,12 @@ def to_dev_bf16(a):
     return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda()
 
 
-def make_stack(cfg: Config, max_tokens=512, prewarm=1, pool=None):
-    """A MoELayerStack with routers, pool (and shared experts) loaded."""
+def make_stack(cfg: Config, max_tokens=512, prewarm=1, pool=None, **opts):
+    """A MoELayerStack with routers, pool (and shared experts) loaded; `opts` go to create."""
     import torch
     from expert_cached_routed_router_b300 import MoELayerStack
     st = MoELayerStack(cfg.L, cfg.E, cfg.k, cfg.d, cfg.d_ff, cfg.n_slots, n_shared=cfg.n_shared,
-                       prewarm=prewarm, max_tokens=max_tokens)
+                       prewarm=prewarm, max_tokens=max_tokens, **opts)
     for l in range(cfg.L):
         st.load_router(l, to_dev_bf16(cfg.router(l)))
         if cfg.n_shared:

@@ -62,5 +62,9 @@ def test_null_handle_is_rejected():
 
 
 def test_options_struct_layout_matches_header():
-    assert ctypes.sizeof(ftm.ft_moe_opts) == 16
+    hdr = open(os.path.join(ROOT, "include", "ft_moe.h")).read()
+    body = re.search(r"typedef struct \{(.*?)\} ft_moe_opts;", hdr, re.S).group(1)
+    names = re.findall(r"^\s*int (\w+);", body, re.M)
+    assert [f for f, _ in ftm.ft_moe_opts._fields_] == names
+    assert ctypes.sizeof(ftm.ft_moe_opts) == 4 * len(names)
     assert ctypes.sizeof(ftm.ft_cache_stats_t) == 8 * 8 + 4 * 4

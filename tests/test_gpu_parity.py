@@ -185,6 +185,75 @@ def test_prefill_double_buffer_matches_oracle():
         np.testing.assert_array_equal(a, b)
     c, k, w = st.prefill_timing()
     assert c > 0 and k > 0 and w > 0
+    assert st.prefill_bytes() == (3 * cfg.E * cfg.entry_bytes, 0)
+    st.close()
+
+
+def test_prefill_topup_from_cache_slots():
+    """Prefill top-up: entries the decode cache holds are copied slot -> buffer, the rest from
+    the host.  Decode calls first scatter layers 2-3 over arbitrary slots (state followed by
+    the oracle simulator); the prefill's outputs then match the oracle on every layer, the
+    cache is unchanged, and the bytes split exactly as the simulator's table says."""
+    import torch
+    cfg = Config(L=4, E=16, k=2, d=256, d_ff=128, n_slots=20, seed=9)
+    T = 300
+    st = make_stack(cfg, max_tokens=T, prefill_topup=1)
+    sim = olru.SlotCacheSim(cfg.L, cfg.E, cfg.n_slots, cfg.entry_bytes, prewarm=True)
+    for step in range(4):
+        x = ft_synth.activations(9, 100 + step, 4, cfg.d)
+        for l in (3, 2):
+            _run(st, l, x)
+            ref = oracle_layer(cfg, l, x, tokens=[])
+            assert sim.access(l, ref["idx"].ravel())[0] == olru.OK
+    assert_cache_equal(st, sim)
+    before = st.cache_state()
+    resident = (sim.table >= 0).sum(axis=1)
+    assert resident.min() < cfg.E and resident[2:].sum() > 0   # a mix of both kinds of copy
+    x = ft_synth.activations(9, 0, T, cfg.d)
+    out = torch.empty((cfg.L, T, cfg.d), dtype=torch.int16, device="cuda")
+    st.prefill(0, cfg.L, to_dev_bf16(x), out)
+    torch.cuda.synchronize()
+    rows = np.arange(1, T, 7)
+    for l in range(cfg.L):
+        ref = oracle_layer(cfg, l, x, tokens=rows)
+        assert_out_close(out_bits_to_f64(out[l])[rows], ref["out"])
+    after = st.cache_state()
+    for a, b in zip(before, after):
+        np.testing.assert_array_equal(a, b)
+    n_res = int(resident.sum())
+    assert st.prefill_bytes() == ((cfg.L * cfg.E - n_res) * cfg.entry_bytes,
+                                  n_res * cfg.entry_bytes)
+    st.close()
+
+
+@pytest.mark.parametrize("T", [1, 4, 40])
+def test_chained_layers_read_previous_output(T):
+    """Layer l+1 takes layer l's output as its input, enqueued back to back with no host
+    synchronisation, so each call's first kernels may start while the previous call's last
+    kernel is still running.  Every layer matches the oracle applied to the GPU's own input
+    (teacher forcing); the cache state after the chain matches the simulator."""
+    import torch
+    cfg = Config(L=5, E=16, k=2, d=256, d_ff=128, n_slots=10, seed=11)
+    st = make_stack(cfg, max_tokens=64)
+    sim = olru.SlotCacheSim(cfg.L, cfg.E, cfg.n_slots, cfg.entry_bytes, prewarm=True)
+    x0 = to_dev_bf16(ft_synth.activations(11, T, T, cfg.d))
+    outs = [torch.empty_like(x0) for _ in range(cfg.L)]
+    for rep in range(3):
+        xin = x0
+        for l in range(cfg.L):
+            st.forward(l, xin, outs[l])
+            xin = outs[l]
+        torch.cuda.synchronize()
+        xin_bits = x0.cpu().numpy().view(np.uint16)
+        for l in range(cfg.L):
+            ref = oracle_layer(cfg, l, xin_bits)
+            assert sim.access(l, ref["idx"].ravel())[0] == olru.OK
+            got = outs[l].cpu().numpy().view(np.uint16)
+            assert_out_close(out_bits_to_f64(outs[l]), ref["out"])
+            xin_bits = got
+        assert_routing_equal(st, ref, T)   # the last call's routing
+        assert_cache_equal(st, sim)
+    assert st.stats()["status"] == 0 and sim.misses > 0
     st.close()
 
 
