@@ -165,7 +165,7 @@ def make_stack(wl, pool, seed, max_tokens, n_slots=None):
     from expert_cached_routed_router_b300 import MoELayerStack
     st = MoELayerStack(wl["L"], wl["E"], wl["k"], wl["d"], wl["d_ff"],
                        n_slots or wl["n_slots"], n_shared=wl["shared"], max_tokens=max_tokens,
-                       prefill_topup=wl.get("topup", 0))
+                       prefill_topup=wl.get("topup", 0), admission=wl.get("admission", 0))
     for l in range(wl["L"]):
         wr = ft_synth.router_weight(seed, l, wl["E"], wl["d"])
         st.load_router(l, torch.from_numpy(wr.view(np.int16)).cuda())
@@ -252,7 +252,7 @@ def bench_decode_batch(wl, pool, b, W, K, seed, world):
     dm = st1["misses"] - st0["misses"]
     res = dict(b=b, ms=ms, ms_per_step=ms / K, tok_s=b * K / (ms / 1e3), hits=dh, misses=dm,
                hit_rate=dh / max(1, dh + dm), fill_bytes=st1["fill_bytes"] - st0["fill_bytes"],
-               clocks=clk.summary())
+               bypasses=st1["bypasses"] - st0["bypasses"], clocks=clk.summary())
     del g
     st.close()
     return res, x_all, bias_all
@@ -422,7 +422,8 @@ def run_decode(args, wl, rank, world):
             "peak_source": pk["source"],
             "algorithmic_bytes": "touched experts x 2*d_ff*d*2 B per call (50.33 MB at b=1)"}
     line = {
-        "metric": "MoE-layer tokens/s (decode trace, b=1)",
+        "metric": "MoE-layer tokens/s (decode trace, b=1"
+                  + (", frequency admission)" if wl.get("admission") else ")"),
         "value": round(res["tok_s_all"], 2), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(res["ms"] / args.steps, 4), "higher_is_better": True,
@@ -430,6 +431,7 @@ def run_decode(args, wl, rank, world):
         "config": {"workload": args.workload, "layers": wl["L"], "d": wl["d"],
                    "d_ff": wl["d_ff"], "experts": wl["E"], "top_k": wl["k"],
                    "n_slots": wl["n_slots"], "batch": b, "graph": True,
+                   "admission": bool(wl.get("admission")),
                    "l2": "inputs larger than L2 (every step streams >1.8 GB of experts)",
                    "parallelism": f"replicas x{world}",
                    "per_batch": {str(bb): {k: (round(v, 4) if isinstance(v, float) else v)
@@ -559,7 +561,18 @@ def run_policy(args, wl, rank, world):
                 hot.access(l, idx.ravel())
         s = st.stats()
         st.close()
+        # the same trace through the device cache with frequency admission (every miss,
+        # cached or staged, crosses the host link)
+        sta = make_stack(dict(wl, admission=1), pool, seed, max_tokens=16)
+        for t in range(n):
+            sta.set_router_bias(-1, bias_all[t])
+            for l in range(L):
+                sta.forward(l, x_all[t], out)
+        sa = sta.stats()
+        sta.close()
         res[str(b)] = {"lru_miss_rate": round(s["misses"] / max(1, s["hits"] + s["misses"]), 4),
+                       "lru_admission_miss_rate": round(sa["misses"] / max(1, sa["hits"] + sa["misses"]), 4),
+                       "lru_admission_bypass_share": round(sa["bypasses"] / max(1, sa["misses"]), 4),
                        "static_layer_split_miss_rate": round(miss_rate(static), 4),
                        "refreshed_hot_set_miss_rate": round(miss_rate(hot), 4),
                        "accesses": s["hits"] + s["misses"]}
@@ -716,6 +729,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batches", default="", help="comma list of decode batch sizes")
     ap.add_argument("--slots", type=int, default=0, help="override the slot count")
+    ap.add_argument("--admission", action="store_true",
+                    help="frequency admission: misses that would displace a more frequently "
+                         "used entry are staged for one call instead of cached")
     ap.add_argument("--experts", type=int, default=0, help="override E (profiling cases)")
     ap.add_argument("--layers", type=int, default=0, help="override L (profiling cases)")
     ap.add_argument("--tokens", default="", help="prefill token counts, comma list")
@@ -729,6 +745,8 @@ def main():
             wl["headline_b"] = wl["batches"][0]
     if args.slots:
         wl["n_slots"] = args.slots
+    if args.admission:
+        wl["admission"] = 1
     if args.experts:
         wl["E"] = args.experts
     if args.layers:

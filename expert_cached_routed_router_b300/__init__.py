@@ -43,7 +43,7 @@ class FtError(RuntimeError):
 class ft_moe_opts(ctypes.Structure):
     _fields_ = [("n_shared", ctypes.c_int), ("prewarm", ctypes.c_int),
                 ("max_tokens", ctypes.c_int), ("debug_checks", ctypes.c_int),
-                ("prefill_topup", ctypes.c_int)]
+                ("prefill_topup", ctypes.c_int), ("admission", ctypes.c_int)]
 
 
 class ft_cache_stats_t(ctypes.Structure):
@@ -51,6 +51,7 @@ class ft_cache_stats_t(ctypes.Structure):
                 ("misses", ctypes.c_uint64), ("fill_bytes", ctypes.c_uint64),
                 ("evictions", ctypes.c_uint64), ("near_ties", ctypes.c_uint64),
                 ("resizes", ctypes.c_uint64), ("tick", ctypes.c_uint64),
+                ("bypasses", ctypes.c_uint64),
                 ("n_slots", ctypes.c_int32), ("occupied", ctypes.c_int32),
                 ("status", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
@@ -140,9 +141,9 @@ def _stream(stream) -> int | None:
 # -------- functions with the C names (marshalling only) ----------------------------------
 
 def ft_moe_create(L, E, k, d, d_ff, n_slots, n_shared=0, prewarm=1, max_tokens=4096,
-                  debug_checks=0, prefill_topup=0) -> int:
+                  debug_checks=0, prefill_topup=0, admission=0) -> int:
     lib = load_library()
-    opts = ft_moe_opts(n_shared, prewarm, max_tokens, debug_checks, prefill_topup)
+    opts = ft_moe_opts(n_shared, prewarm, max_tokens, debug_checks, prefill_topup, admission)
     h = ctypes.c_void_p()
     _check(lib.ft_moe_create(L, E, k, d, d_ff, n_slots, ctypes.byref(opts), ctypes.byref(h)))
     return h.value
@@ -295,12 +296,12 @@ class MoELayerStack:
     """One ft_moe handle: L routed-MoE layers sharing one LRU expert-slot cache."""
 
     def __init__(self, L, E, k, d, d_ff, n_slots, n_shared=0, prewarm=1, max_tokens=4096,
-                 debug_checks=0, prefill_topup=0):
+                 debug_checks=0, prefill_topup=0, admission=0):
         self.L, self.E, self.k, self.d, self.d_ff = L, E, k, d, d_ff
         self.n_shared = n_shared
         self.entry_elems = 3 * d * d_ff
         self.h = ft_moe_create(L, E, k, d, d_ff, n_slots, n_shared, prewarm, max_tokens,
-                               debug_checks, prefill_topup)
+                               debug_checks, prefill_topup, admission)
 
     def close(self):
         if self.h:

@@ -36,6 +36,8 @@ constexpr double kNearTie = 1e-6;  // top-k gap reported as a near-tie (exact fp
 struct DevCounters {
   unsigned long long calls, hits, misses, fill_bytes, evictions, near_ties;
   unsigned long long tick;       // global LRU clock
+  unsigned long long bypasses;   // misses staged without entering the cache (admission)
+  unsigned long long acc;        // admission: accesses since the counts were last halved
   int status;                    // first device-side error (FT_ERR_*), 0 = none
   int n_fill;                    // fills of the most recent forward call
   int n_work;                    // work items of the most recent call
@@ -85,6 +87,7 @@ struct ControlArgs {
   int32_t *slot_table;  // [L][E]
   const CacheDesc *cache;      // slot storage, owners, stamps, capacity (device)
   int32_t *fills;       // [max_fill][3]
+  uint32_t *freq;       // admission counts [L][E], or null for the plain LRU
   const uint16_t *buffer;      // prefill: E entries of this layer
   const uint16_t *shared;      // shared entry of this layer or null
   size_t entry_elems;

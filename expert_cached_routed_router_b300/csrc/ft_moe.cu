@@ -99,6 +99,9 @@ struct ft_moe {
   std::vector<cudaEvent_t> ev_cs, ev_ce, ev_ks, ev_ke;  // copy start/end, compute start/end
   int last_prefill_layers = 0;
   int prefill_topup = 0;
+  int admission = 0;          // frequency admission (see ft_moe_opts)
+  int n_stage = 0;            // staging entries after the slots: E with admission, else 0
+  uint32_t *freq = nullptr;   // admission counts [L][E]
   uint64_t last_h2d_bytes = 0, last_d2d_bytes = 0;  // moved by the last prefill
   std::vector<int32_t> table_host;                  // slot table read by the top-up
 
@@ -235,6 +238,7 @@ ControlArgs control_args(ft_moe *h, int layer, int T, bool decode, const uint16_
   a.slot_table = decode ? h->slot_table : nullptr;
   a.cache = h->cache;
   a.fills = h->fills;
+  a.freq = h->freq;
   a.buffer = buffer;
   a.shared = h->n_shared ? h->shared + (size_t)layer * h->entry_elems : nullptr;
   a.entry_elems = h->entry_elems;
@@ -357,7 +361,7 @@ int ft_moe_create(int L, int E, int k, int d, int d_ff, int n_slots, const ft_mo
                 "need d in [128, 4096] and d_ff in [128, 8192], multiples of 128 (got %d, %d)", d,
                 d_ff);
   if (n_slots < 1) return fail(FT_ERR_INVALID, "n_slots must be >= 1 (got %d)", n_slots);
-  ft_moe_opts o{0, 1, 4096, 0, 0};
+  ft_moe_opts o{0, 1, 4096, 0, 0, 0};
   if (opts) o = *opts;
   if (o.max_tokens < 1 || o.max_tokens > (1 << 20))
     return fail(FT_ERR_INVALID, "max_tokens out of range (%d)", o.max_tokens);
@@ -375,6 +379,8 @@ int ft_moe_create(int L, int E, int k, int d, int d_ff, int n_slots, const ft_mo
   h->prewarm = o.prewarm;
   h->debug = o.debug_checks;
   h->prefill_topup = o.prefill_topup != 0;
+  h->admission = o.admission != 0;
+  h->n_stage = h->admission ? E : 0;
   h->entry_elems = (size_t)3 * d * d_ff;
   h->entry_bytes = h->entry_elems * 2;
   h->has_bias.assign(L, 0);
@@ -409,8 +415,9 @@ int ft_moe_create(int L, int E, int k, int d, int d_ff, int n_slots, const ft_mo
   A(alloc_n(h, &h->ybuf, (size_t)(kGemvMaxTokens * k + kGemvMaxTokens) * d));
   A(alloc_n(h, &h->chunk, perm_multi_scratch_ints((int)P, E)));
   A(alloc_n(h, &h->tile_prefix, (size_t)kMaxE + 3));
+  if (h->admission) A(alloc_n(h, &h->freq, (size_t)L * E));
   if (rc == FT_OK) {
-    cudaError_t e = cudaMalloc(&h->slots, (size_t)n_slots * h->entry_bytes);
+    cudaError_t e = cudaMalloc(&h->slots, (size_t)(n_slots + h->n_stage) * h->entry_bytes);
     if (e == cudaSuccess) e = cudaMalloc(&h->owner, (size_t)n_slots * sizeof(int32_t));
     if (e == cudaSuccess) e = cudaMalloc(&h->stamps, (size_t)n_slots * sizeof(unsigned long long));
     if (e != cudaSuccess) {
@@ -426,13 +433,14 @@ int ft_moe_create(int L, int E, int k, int d, int d_ff, int n_slots, const ft_mo
     if (e == cudaSuccess) e = cudaMemset(h->owner, 0xFF, (size_t)n_slots * sizeof(int32_t));
     if (e == cudaSuccess) e = cudaMemset(h->stamps, 0, (size_t)n_slots * sizeof(unsigned long long));
     if (e == cudaSuccess) e = cudaMemset(h->ctr, 0, sizeof(DevCounters));
+    if (e == cudaSuccess && h->freq) e = cudaMemset(h->freq, 0, (size_t)L * E * sizeof(uint32_t));
     if (e == cudaSuccess) e = cudaMemset(h->wr, 0, (size_t)L * E * d * 2);
     if (e == cudaSuccess && h->shared) e = cudaMemset(h->shared, 0, (size_t)L * h->entry_bytes);
     if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&h->copy_stream, cudaStreamNonBlocking);
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (e != cudaSuccess) rc = fail(FT_ERR_CUDA, "initialisation: %s", cudaGetErrorString(e));
   }
-  if (rc == FT_OK) rc = build_maps(h, &h->maps_slots, h->slots, n_slots);
+  if (rc == FT_OK) rc = build_maps(h, &h->maps_slots, h->slots, n_slots + h->n_stage);
   if (rc == FT_OK) rc = upload_cache_desc(h);
   if (rc != FT_OK) {
     free_all(h);
@@ -768,7 +776,7 @@ int ft_cache_resize(ft_moe *h, int n_new) {
   unsigned long long *nstamps = nullptr;
   cudaError_t e = cudaSuccess;
   if (inject("resize_alloc")) e = cudaErrorMemoryAllocation;
-  if (e == cudaSuccess) e = cudaMalloc(&nslots, (size_t)n_new * h->entry_bytes);
+  if (e == cudaSuccess) e = cudaMalloc(&nslots, (size_t)(n_new + h->n_stage) * h->entry_bytes);
   if (e == cudaSuccess) e = cudaMalloc(&nowner, (size_t)n_new * 4);
   if (e == cudaSuccess) e = cudaMalloc(&nstamps, (size_t)n_new * 8);
   if (e != cudaSuccess) {
@@ -808,7 +816,7 @@ int ft_cache_resize(ft_moe *h, int n_new) {
   h->stamps = nstamps;
   h->n_slots = n_new;
   if (int r = upload_cache_desc(h)) return r;
-  if (int r = build_maps(h, &h->maps_slots, h->slots, n_new)) return r;
+  if (int r = build_maps(h, &h->maps_slots, h->slots, n_new + h->n_stage)) return r;
   DevCounters c{};
   FT_CUDA(cudaMemcpy(&c, h->ctr, sizeof(c), cudaMemcpyDeviceToHost));
   c.occupied = m;
@@ -832,6 +840,7 @@ int ft_cache_stats(ft_moe *h, ft_cache_stats_t *out) {
   out->near_ties = c.near_ties;
   out->resizes = h->resizes;
   out->tick = c.tick;
+  out->bypasses = c.bypasses;
   out->n_slots = h->n_slots;
   out->occupied = c.occupied;
   out->status = c.status;
@@ -843,7 +852,7 @@ int ft_cache_stats_reset(ft_moe *h) {
   FT_CUDA(cudaDeviceSynchronize());
   DevCounters c{};
   FT_CUDA(cudaMemcpy(&c, h->ctr, sizeof(c), cudaMemcpyDeviceToHost));
-  c.calls = c.hits = c.misses = c.fill_bytes = c.evictions = c.near_ties = 0;
+  c.calls = c.hits = c.misses = c.fill_bytes = c.evictions = c.near_ties = c.bypasses = 0;
   c.status = 0;
   FT_CUDA(cudaMemcpy(h->ctr, &c, sizeof(c), cudaMemcpyHostToDevice));
   h->resizes = 0;

@@ -335,6 +335,10 @@ void launch_perm_multi(const ControlArgs &a, int32_t *chunk_scratch, cudaStream_
 //      after the hits'; every miss is appended to the fill list.  |S| > n_slots sets
 //      FT_ERR_CAPACITY and leaves the cache and the outputs untouched.
 //      prefill: expert e reads entry e of the layer's double buffer.
+//      With admission counts (a.freq), every touched key's count grows by one and all counts
+//      are halved once 10 * n_slots accesses have accumulated; a miss that finds no free
+//      slot takes the next victim only if its count is >= the victim's, else it is staged
+//      for this call in entry n_slots + b and the cache does not change.
 //   3. the work list (touched experts ascending, then the shared expert) and counters.
 // Threads leave data-dependent loops at different times; every block barrier that may
 // follow such a loop is preceded by __syncwarp() (cta_sync), so warps reach it converged.
@@ -345,7 +349,10 @@ constexpr int kPairSmem = kGemvMaxTokens * kMaxK;    // pairs of the in-CTA top-
 constexpr int kFieldBits = 21;                       // packed per-expert scan fields
 constexpr unsigned long long kFieldMask = (1ull << kFieldBits) - 1;
 
-enum { kMiscNear = 0, kMiscDigit, kMiscNeed, kMiscCand, kMiscErr, kMiscN };
+enum {
+  kMiscNear = 0, kMiscDigit, kMiscNeed, kMiscCand, kMiscErr,
+  kMiscHalve, kMiscAdmit, kMiscEvict, kMiscBypass, kMiscN
+};
 
 struct CtlSmem {
   int cnt[kMaxE];
@@ -361,6 +368,12 @@ struct CtlSmem {
   union {
     float logit[kTopkSmem];
     unsigned long long key[kStampSmem];
+    struct {              // admission decisions, by miss rank m / victim rank j
+      unsigned mf[kMaxE];   // count of miss m
+      unsigned vf[kMaxE];   // count of victim j's key
+      int dest[kMaxE];      // slot, or staging entry n_slots + b
+      int rank[kMaxE];      // stamp rank among admitted misses, -1 = bypassed
+    } adm;
   } u;
 };
 
@@ -680,6 +693,20 @@ __device__ __forceinline__ void control_body(const ControlArgs &a, int mode,
       return;
     }
     const unsigned long long tick0 = a.ctr->tick;
+    if (a.freq) {
+      if (touched) a.freq[(size_t)a.layer * E + tid] += 1u;
+      if (tid == 0) {
+        unsigned long long acc = a.ctr->acc + (unsigned long long)n_touched;
+        const unsigned long long H = 10ull * (unsigned long long)cd.n_slots;
+        sm.misc[kMiscHalve] = acc >= H ? 1 : 0;
+        a.ctr->acc = acc >= H ? acc - H : acc;
+      }
+      cta_sync();
+      if (sm.misc[kMiscHalve]) {
+        for (int i = tid; i < a.L * E; i += 1024) a.freq[i] >>= 1;
+        cta_sync();
+      }
+    }
     if (hit) {
       if (cur < cd.n_slots)
         cd.stamps[cur] = tick0 + 1 + (unsigned long long)hrank;
@@ -687,6 +714,8 @@ __device__ __forceinline__ void control_body(const ControlArgs &a, int mode,
         set_status(a.ctr, FT_ERR_INVALID);
     }
     int n_free = 0;
+    int n_admit = n_miss, n_evict = 0, n_bypass = 0;
+    bool decided = false;  // admission decisions in sm.u.adm
     if (n_miss > 0) {
       cta_sync();  // hit stamps written before eviction keys are read
       // the n_miss lowest free slots (none to look for once every slot is occupied)
@@ -712,17 +741,51 @@ __device__ __forceinline__ void control_body(const ControlArgs &a, int mode,
         return;
       }
       cta_sync();
+      n_evict = nv;
+      if (a.freq && nv > 0) {
+        // misses in ascending expert id: a free slot while any is left, else the next victim
+        // if the miss's count is at least the victim key's, else a staging entry
+        if (miss) sm.u.adm.mf[mrank] = a.freq[(size_t)a.layer * E + tid];
+        if (tid < nv) sm.u.adm.vf[tid] = a.freq[cd.owner[sm.slot[n_free + tid]]];
+        cta_sync();
+        if (tid == 0) {
+          int j = 0, b = 0, r = 0;
+          for (int m = 0; m < n_miss; ++m) {
+            if (m < n_free) {
+              sm.u.adm.dest[m] = sm.slot[m];
+              sm.u.adm.rank[m] = r++;
+            } else if (j < nv && sm.u.adm.mf[m] >= sm.u.adm.vf[j]) {
+              sm.u.adm.dest[m] = sm.slot[n_free + j++];
+              sm.u.adm.rank[m] = r++;
+            } else {
+              sm.u.adm.dest[m] = cd.n_slots + b++;
+              sm.u.adm.rank[m] = -1;
+            }
+          }
+          sm.misc[kMiscAdmit] = r;
+          sm.misc[kMiscEvict] = j;
+          sm.misc[kMiscBypass] = b;
+        }
+        cta_sync();
+        n_admit = sm.misc[kMiscAdmit];
+        n_evict = sm.misc[kMiscEvict];
+        n_bypass = sm.misc[kMiscBypass];
+        decided = true;
+      }
     }
     if (miss) {
       const int m = mrank;
-      const int slot = sm.slot[m];
-      if (m >= n_free) {
-        const int ev = cd.owner[slot];
-        if (ev >= 0 && ev < a.L * E) a.slot_table[ev] = -1;
+      const int slot = decided ? sm.u.adm.dest[m] : sm.slot[m];
+      const int arank = decided ? sm.u.adm.rank[m] : m;
+      if (arank >= 0) {
+        if (m >= n_free) {
+          const int ev = cd.owner[slot];
+          if (ev >= 0 && ev < a.L * E) a.slot_table[ev] = -1;
+        }
+        cd.owner[slot] = a.layer * E + tid;
+        table[tid] = slot;
+        cd.stamps[slot] = tick0 + (unsigned long long)n_hit + 1ull + (unsigned long long)arank;
       }
-      cd.owner[slot] = a.layer * E + tid;
-      table[tid] = slot;
-      cd.stamps[slot] = tick0 + (unsigned long long)n_hit + 1ull + (unsigned long long)m;
       a.fills[3 * m + 0] = slot;
       a.fills[3 * m + 1] = a.layer;
       a.fills[3 * m + 2] = tid;
@@ -731,14 +794,15 @@ __device__ __forceinline__ void control_body(const ControlArgs &a, int mode,
       slot_of = cur;
     }
     if (tid == 0) {
-      a.ctr->tick = tick0 + (unsigned long long)(n_hit + n_miss);
+      a.ctr->tick = tick0 + (unsigned long long)(n_hit + n_admit);
       a.ctr->calls += 1;
       a.ctr->hits += (unsigned long long)n_hit;
       a.ctr->misses += (unsigned long long)n_miss;
       a.ctr->fill_bytes += (unsigned long long)n_miss * a.entry_elems * 2ull;
-      a.ctr->evictions += (unsigned long long)nv;
+      a.ctr->evictions += (unsigned long long)n_evict;
+      a.ctr->bypasses += (unsigned long long)n_bypass;
       a.ctr->n_fill = n_miss;
-      a.ctr->occupied += n_miss - nv;
+      a.ctr->occupied += n_admit - n_evict;
     }
   } else {
     slot_of = touched ? tid : -1;

@@ -67,6 +67,9 @@ typedef struct {
   int debug_checks; /* [0] kernels re-check slot indices and record violations           */
   int prefill_topup; /* [0] 1 = prefill copies entries already resident in cache slots
                             device -> device and streams only the rest from the host      */
+  int admission;     /* [0] 1 = frequency admission: a miss that finds no free slot replaces
+                            the next LRU victim only if its access count is at least the
+                            victim's, else it is staged for the one call (see below)       */
 } ft_moe_opts;
 
 /* Cache counters, accumulated on the device since creation or the last reset. */
@@ -79,6 +82,7 @@ typedef struct {
   uint64_t near_ties;  /* tokens whose top-k decision had a logit gap <= 1e-6             */
   uint64_t resizes;    /* successful ft_cache_resize calls                                */
   uint64_t tick;       /* global LRU clock (last stamp handed out)                        */
+  uint64_t bypasses;   /* misses staged for one call without entering the cache          */
   int32_t n_slots;     /* current capacity in entries                                     */
   int32_t occupied;    /* slots holding an entry                                          */
   int32_t status;      /* first device-side error code since the last reset (0 = none)    */

@@ -67,4 +67,8 @@ def test_options_struct_layout_matches_header():
     names = re.findall(r"^\s*int (\w+);", body, re.M)
     assert [f for f, _ in ftm.ft_moe_opts._fields_] == names
     assert ctypes.sizeof(ftm.ft_moe_opts) == 4 * len(names)
-    assert ctypes.sizeof(ftm.ft_cache_stats_t) == 8 * 8 + 4 * 4
+    body = re.search(r"typedef struct \{(.*?)\} ft_cache_stats_t;", hdr, re.S).group(1)
+    fields = re.findall(r"^\s*(uint64_t|int32_t) (\w+);", body, re.M)
+    assert [f for f, _ in ftm.ft_cache_stats_t._fields_] == [n for _, n in fields]
+    assert ctypes.sizeof(ftm.ft_cache_stats_t) == sum(8 if t == "uint64_t" else 4
+                                                     for t, _ in fields)

@@ -27,10 +27,11 @@ def _gpu_pool(seed, L, E, d, d_ff):
     return pool
 
 
-def _stack(pool, seed, L, E, k, d, d_ff, n_slots, max_tokens, shared=0):
+def _stack(pool, seed, L, E, k, d, d_ff, n_slots, max_tokens, shared=0, admission=0):
     import torch
     from expert_cached_routed_router_b300 import MoELayerStack
-    st = MoELayerStack(L, E, k, d, d_ff, n_slots, n_shared=shared, max_tokens=max_tokens)
+    st = MoELayerStack(L, E, k, d, d_ff, n_slots, n_shared=shared, max_tokens=max_tokens,
+                       admission=admission)
     for l in range(L):
         st.load_router(l, torch.from_numpy(ft_synth.router_weight(seed, l, E, d).view(np.int16)).cuda())
         if shared:
@@ -47,13 +48,16 @@ def _entry_view(pool, L, E, d, d_ff):
 
 
 def _decode_trace_parity(seed, L, E, k, d, d_ff, n_slots, zipf, b, n_steps, out_every, shared=0,
-                         phase_len=0, resizes=(), pool=None, batch_of=None, out_tokens=4):
+                         phase_len=0, resizes=(), pool=None, batch_of=None, out_tokens=4,
+                         admission=0):
     """Run a decode trace; compare every call bit-exactly, sampled outputs within tolerance."""
     import torch
     pool = _gpu_pool(seed, L, E, d, d_ff) if pool is None else pool
-    st = _stack(pool, seed, L, E, k, d, d_ff, n_slots, max_tokens=16, shared=shared)
+    st = _stack(pool, seed, L, E, k, d, d_ff, n_slots, max_tokens=16, shared=shared,
+                admission=admission)
     entry = _entry_view(pool, L, E, d, d_ff)
-    sim = olru.SlotCacheSim(L, E, n_slots, 6 * d * d_ff, prewarm=True)
+    sim = olru.SlotCacheSim(L, E, n_slots, 6 * d * d_ff, prewarm=True,
+                            admission=bool(admission))
     gen = ft_synth.DriftingZipfBias(seed, L, E, s=zipf, phase_len=phase_len)
     routers = [ft_synth.router_weight(seed, l, E, d) for l in range(L)]
     w_stack = np.concatenate(routers, axis=0)     # every layer's experts, one oracle call
@@ -114,7 +118,7 @@ def _decode_trace_parity(seed, L, E, k, d, d_ff, n_slots, zipf, b, n_steps, out_
                 checked_out += 1
     s = st.stats()
     assert s["hits"] == sim.hits and s["misses"] == sim.misses and s["status"] == 0
-    assert s["evictions"] == sim.evictions
+    assert s["evictions"] == sim.evictions and s["bypasses"] == sim.bypasses
     st.close()
     return sim, checked_out
 
@@ -124,6 +128,14 @@ def test_decode_trace_24_layers():
     sim, n_out = _decode_trace_parity(0, 24, 128, 8, 2048, 768, 768, 1.1, b=4, n_steps=60,
                                       out_every=20)
     assert sim.misses > 0 and sim.evictions > 0 and n_out == 6
+
+
+def test_decode_trace_24_layers_admission():
+    """The same 24-layer trace with frequency admission: bypassed misses are staged past the
+    768 slots; fills, cache state and counters bit-exact, outputs within tolerance."""
+    sim, n_out = _decode_trace_parity(0, 24, 128, 8, 2048, 768, 768, 1.1, b=4, n_steps=60,
+                                      out_every=20, admission=1)
+    assert sim.bypasses > 0 and n_out == 6
 
 
 def test_elastic_resize_trace():
