@@ -415,7 +415,7 @@ def run_decode(args, wl, rank, world):
     g = rl["gateup"]
     # DRAM bytes per launch of k_gateup_tma at b = 1 (8 touched experts) from the committed ncu
     # capture (profiles/decode_kernels_full_capture.md); only valid for that shape
-    traffic = 50.47e6 if (args.workload == "decode24" and b == 1) else None  # ncu, per launch
+    traffic = 50.56e6 if (args.workload == "decode24" and b == 1) else None  # ncu, per launch
     roof = {"bound": "hbm", "kernel": "k_gateup_tma (gate/up + SwiGLU, decode)",
             "achieved": round(g["achieved"], 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
             "frac": round(g["achieved"] / pk["hbm_gbs"], 4), "traffic": traffic,
