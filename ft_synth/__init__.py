@@ -38,6 +38,7 @@ TAG_POOL = 3       # routed expert entry (l, e)
 TAG_SHARED = 4     # shared expert entry of layer l
 TAG_DRIFT = 5      # random-walk increments of the router bias
 TAG_PERM = 6       # per-layer popularity order
+TAG_POOL_FP4 = 7   # routed expert entry (l, e), 4-bit codes and block scales
 
 ENTRY_SIGMA = 0.02
 ROUTER_SIGMA = 0.02
@@ -118,6 +119,29 @@ def expert_entry(seed: int, layer: int, expert: int, d: int, d_ff: int,
     """
     n = entry_elems(d, d_ff) - start if n is None else n
     return normal_bf16(stream_key(seed, TAG_POOL, layer, expert), n, ENTRY_SIGMA, start)
+
+
+def entry_bytes_fp4(d: int, d_ff: int) -> int:
+    """Bytes of one 4-bit entry: 3*d*d_ff codes of 4 bits plus one scale byte per 32."""
+    return 3 * d * d_ff * 17 // 32
+
+
+def expert_entry_fp4(seed: int, layer: int, expert: int, d: int, d_ff: int) -> np.ndarray:
+    """Packed 4-bit entry of routed expert (layer, expert) as uint8 [entry_bytes_fp4].
+
+    The first 3*d*d_ff/2 bytes (the codes) are the little-endian bytes of draws
+    0 .. 3*d*d_ff/16 - 1 of the stream, so every 4-bit code is uniform over its 16 values;
+    the remaining 3*d*d_ff/32 bytes (the block scales) are 118 + (draw mod 3) of the draws
+    that follow, one draw per byte.  The layout of the regions is the 4-bit entry layout
+    (codes of W_gate, W_up, W_down, then their scales); interpreting it is the oracle's and
+    the kernels' business.
+    """
+    key = stream_key(seed, TAG_POOL_FP4, layer, expert)
+    nc = 3 * d * d_ff // 2
+    ns = 3 * d * d_ff // 32
+    codes = draws(key, 0, nc // 8).astype("<u8").view(np.uint8)
+    scales = (np.uint64(118) + draws(key, nc // 8, ns) % np.uint64(3)).astype(np.uint8)
+    return np.concatenate([codes, scales])
 
 
 def shared_entry(seed: int, layer: int, d: int, d_ff: int) -> np.ndarray:

@@ -156,6 +156,11 @@ def expert_ffn(x_f64, entry_bits, d: int, d_ff: int) -> np.ndarray:
     wg = bf16_to_f64(e[:n]).reshape(d_ff, d)
     wu = bf16_to_f64(e[n:2 * n]).reshape(d_ff, d)
     wd = bf16_to_f64(e[2 * n:3 * n]).reshape(d, d_ff)
+    return swiglu_rows(x_f64, wg, wu, wd)
+
+
+def swiglu_rows(x_f64, wg, wu, wd) -> np.ndarray:
+    """g = x Wg^T, u = x Wu^T, h = silu(g) * u, y = h Wd^T on rows x [n][d], in float64."""
     x = np.atleast_2d(np.asarray(x_f64, dtype=np.float64))
     g = x @ wg.T
     u = x @ wu.T
@@ -164,12 +169,13 @@ def expert_ffn(x_f64, entry_bits, d: int, d_ff: int) -> np.ndarray:
 
 
 def moe_layer(x_bits, wr_bits, k: int, entry_of, d: int, d_ff: int, bias=None,
-              shared_entry=None, tokens=None):
+              shared_entry=None, tokens=None, ffn=None):
     """One routed MoE layer forward.
 
     x [T][d] bf16, W_r [E][d] bf16, ``entry_of(e)`` -> flat bf16 entry of expert e.
     ``tokens``: optional subset of token rows whose outputs are computed (routing is
-    always computed for all T).  Returns a dict with logits, idx, tie, w, counts,
+    always computed for all T).  ``ffn(x, entry, d, d_ff)``: the expert network of an entry
+    (default ``expert_ffn``, bf16 entries).  Returns a dict with logits, idx, tie, w, counts,
     offsets, perm, inv and ``out`` (float64 [len(tokens)][d]).
     """
     x_bits = np.asarray(x_bits, dtype=np.uint16)
@@ -182,15 +188,16 @@ def moe_layer(x_bits, wr_bits, k: int, entry_of, d: int, d_ff: int, bias=None,
     rows = np.arange(T) if tokens is None else np.asarray(tokens)
     xf = bf16_to_f64(x_bits)
     out = np.zeros((len(rows), d), dtype=np.float64)
+    ffn = expert_ffn if ffn is None else ffn
     cache = {}
     for r, t in enumerate(rows):
         for j in range(k):
             e = int(idx[t, j])
             if e not in cache:
-                cache[e] = np.asarray(entry_of(e), dtype=np.uint16)
-            out[r] += float(w[t, j]) * expert_ffn(xf[t], cache[e], d, d_ff)[0]
+                cache[e] = np.asarray(entry_of(e))
+            out[r] += float(w[t, j]) * ffn(xf[t], cache[e], d, d_ff)[0]
         if shared_entry is not None:
-            out[r] += expert_ffn(xf[t], shared_entry, d, d_ff)[0]
+            out[r] += ffn(xf[t], shared_entry, d, d_ff)[0]
     return dict(logits=logits, idx=idx, tie=tie, w=w, counts=counts, offsets=offsets,
                 perm=perm, inv=inv, out=out, tokens=rows)
 

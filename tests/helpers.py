@@ -41,6 +41,16 @@ def host_pool(cfg: Config):
     return pool
 
 
+def gpu_host_pool(cfg: Config):
+    """The same pool as host_pool, written by the GPU generator (for large L*E)."""
+    import torch
+    import ft_synth.gpu as sg
+    sg.build()
+    pool = torch.empty(cfg.L * cfg.E * cfg.entry_elems, dtype=torch.int16, pin_memory=True)
+    sg.fill_pool(pool.data_ptr(), cfg.seed, cfg.L, cfg.E, cfg.d, cfg.d_ff)
+    return pool
+
+
 def to_dev_bf16(a):
     import torch
     return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda()

@@ -7,7 +7,7 @@ from oracle import lru as olru
 from oracle import moe as omoe
 
 from helpers import (Config, assert_cache_equal, assert_out_close, assert_routing_equal,
-                     make_stack, oracle_layer, out_bits_to_f64, to_dev_bf16)
+                     gpu_host_pool, make_stack, oracle_layer, out_bits_to_f64, to_dev_bf16)
 
 pytestmark = pytest.mark.gpu
 
@@ -51,6 +51,57 @@ def test_layer_token_counts(T):
         assert_routing_equal(st, ref, T)
         assert_out_close(out_bits_to_f64(out), ref["out"])
     assert st.status() == 0
+    st.close()
+
+
+@pytest.mark.parametrize("E,k,T,n_slots", [
+    (512, 8, 16, 200),    # T*E > 4096: the fused decode kernel falls back to warp top-k
+    (1024, 32, 1, 300),   # largest E and k, in-CTA top-k
+    (1024, 32, 4, 300),   # T*E = 4096, the in-CTA limit
+    (1024, 32, 5, 300),   # just past it
+])
+def test_decode_edge_shapes(E, k, T, n_slots):
+    """Decode calls at the limits of the in-CTA top-k and of E and k, with evictions: routing,
+    grouping, fills and the whole cache state bit-exact; outputs within tolerance."""
+    cfg = Config(L=2, E=E, k=k, d=128, d_ff=128, n_slots=n_slots, seed=12)
+    st = make_stack(cfg, max_tokens=16, pool=gpu_host_pool(cfg))
+    sim = olru.SlotCacheSim(cfg.L, cfg.E, cfg.n_slots, cfg.entry_bytes, prewarm=True)
+    for step in range(3):
+        for l in (1, 0):
+            x = ft_synth.activations(12, 1000 * T + 10 * step + l, T, cfg.d)
+            out = _run(st, l, x)
+            ref = oracle_layer(cfg, l, x, tokens=np.arange(min(T, 3)))
+            assert_routing_equal(st, ref, T)
+            code, hits, fills = sim.access(l, ref["idx"].ravel())
+            assert code == olru.OK
+            np.testing.assert_array_equal(st.fills(), np.array([f[:3] for f in fills],
+                                                                dtype=np.int32).reshape(-1, 3))
+            assert_cache_equal(st, sim)
+            assert_out_close(out_bits_to_f64(out)[ref["tokens"]], ref["out"])
+    assert sim.evictions > 0 and st.status() == 0
+    st.close()
+
+
+def test_victims_beyond_shared_memory_staging():
+    """More than 2,048 slots: the control reads the eviction keys from global memory."""
+    cfg = Config(L=40, E=64, k=4, d=128, d_ff=128, n_slots=2100, seed=13)
+    st = make_stack(cfg, max_tokens=16, pool=gpu_host_pool(cfg))
+    sim = olru.SlotCacheSim(cfg.L, cfg.E, cfg.n_slots, cfg.entry_bytes, prewarm=True)
+    for step in range(6):
+        for l in (39, 35, 3):
+            x = ft_synth.activations(13, 10 * step + l, 4, cfg.d)
+            out = _run(st, l, x)
+            want = step % 3 == 0
+            ref = oracle_layer(cfg, l, x, tokens=None if want else [])
+            assert_routing_equal(st, ref, 4)
+            code, hits, fills = sim.access(l, ref["idx"].ravel())
+            assert code == olru.OK
+            np.testing.assert_array_equal(st.fills(), np.array([f[:3] for f in fills],
+                                                                dtype=np.int32).reshape(-1, 3))
+            assert_cache_equal(st, sim)
+            if want:
+                assert_out_close(out_bits_to_f64(out), ref["out"])
+    assert sim.evictions > 0 and st.status() == 0
     st.close()
 
 
