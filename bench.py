@@ -149,10 +149,21 @@ def max_over_ranks(v, world):
 # ----------------------------------------------------------------------------------------
 # workload construction
 # ----------------------------------------------------------------------------------------
+def entry_bytes(wl):
+    """Bytes of one (layer, expert) entry: bf16, or MXFP4 codes + block scales."""
+    n = 3 * wl["d"] * wl["d_ff"]
+    return n * 17 // 32 if wl.get("fp4") else 2 * n
+
+
 def build_pool(wl, seed):
     import torch
     import ft_synth.gpu as sg
     sg.build()
+    if wl.get("fp4"):
+        pool = torch.empty(wl["L"] * wl["E"] * entry_bytes(wl), dtype=torch.uint8,
+                           pin_memory=True)
+        sg.fill_pool_fp4(pool.data_ptr(), seed, wl["L"], wl["E"], wl["d"], wl["d_ff"])
+        return pool
     n = wl["L"] * wl["E"] * 3 * wl["d"] * wl["d_ff"]
     pool = torch.empty(n, dtype=torch.int16, pin_memory=True)
     sg.fill_pool(pool.data_ptr(), seed, wl["L"], wl["E"], wl["d"], wl["d_ff"])
@@ -165,14 +176,15 @@ def make_stack(wl, pool, seed, max_tokens, n_slots=None):
     from expert_cached_routed_router_b300 import MoELayerStack
     st = MoELayerStack(wl["L"], wl["E"], wl["k"], wl["d"], wl["d_ff"],
                        n_slots or wl["n_slots"], n_shared=wl["shared"], max_tokens=max_tokens,
-                       prefill_topup=wl.get("topup", 0), admission=wl.get("admission", 0))
+                       prefill_topup=wl.get("topup", 0), admission=wl.get("admission", 0),
+                       weight_format=1 if wl.get("fp4") else 0)
     for l in range(wl["L"]):
         wr = ft_synth.router_weight(seed, l, wl["E"], wl["d"])
         st.load_router(l, torch.from_numpy(wr.view(np.int16)).cuda())
         if wl["shared"]:
             sh = ft_synth.shared_entry(seed, l, wl["d"], wl["d_ff"])
             st.load_shared(l, torch.from_numpy(sh.view(np.int16)).cuda())
-    st.load_pool(pool, pool.numel() * 2)
+    st.load_pool(pool, pool.numel() * pool.element_size())
     torch.cuda.synchronize()
     return st
 
@@ -331,10 +343,13 @@ def cpu_oracle_decode(wl, pool, b, bias_np, seed, budget_s=15.0, max_calls=None)
     import ft_synth
     from oracle import lru as olru
     from oracle import moe as omoe
+    from oracle import fp4 as ofp4
     L, E, k, d, d_ff = wl["L"], wl["E"], wl["k"], wl["d"], wl["d_ff"]
-    ent = 3 * d * d_ff
-    pv = pool.numpy().view(np.uint16)
-    sim = olru.SlotCacheSim(L, E, wl["n_slots"], 2 * ent, prewarm=True)
+    fp4 = bool(wl.get("fp4"))
+    ent = entry_bytes(wl) if fp4 else 3 * d * d_ff      # pool elements per entry
+    pv = pool.numpy() if fp4 else pool.numpy().view(np.uint16)
+    sim = olru.SlotCacheSim(L, E, wl["n_slots"], entry_bytes(wl), prewarm=True,
+                            admission=bool(wl.get("admission")))
     routers = {}
     calls = 0
     t0 = time.perf_counter()
@@ -348,7 +363,8 @@ def cpu_oracle_decode(wl, pool, b, bias_np, seed, budget_s=15.0, max_calls=None)
                                lambda e, l=l: pv[(l * E + e) * ent:(l * E + e + 1) * ent],
                                d, d_ff, bias=bias_np[step, l],
                                shared_entry=(ft_synth.shared_entry(seed, l, d, d_ff)
-                                             if wl["shared"] else None))
+                                             if wl["shared"] else None),
+                               ffn=ofp4.expert_ffn_fp4 if fp4 else None)
             sim.access(l, r["idx"].ravel())
             calls += 1
             el = time.perf_counter() - t0
@@ -360,8 +376,9 @@ def cpu_oracle_decode(wl, pool, b, bias_np, seed, budget_s=15.0, max_calls=None)
 def roofline_decode(wl, prof, touched, n_calls, pk):
     """Achieved HBM GB/s of the gate/up GEMV (the largest HBM consumer of the step)."""
     d, d_ff = wl["d"], wl["d_ff"]
-    gate_bytes = touched * 2 * d_ff * d * 2
-    down_bytes = touched * d * d_ff * 2
+    per_matrix = entry_bytes(wl) // 3                    # bytes of one d x d_ff matrix
+    gate_bytes = touched * 2 * per_matrix
+    down_bytes = touched * per_matrix
     g_ms, g_n = prof["gateup"]
     dn_ms, dn_n = prof["down"]
     out = {}
@@ -414,25 +431,34 @@ def run_decode(args, wl, rank, world):
                          f"+ fp64 experts, single thread"}
     g = rl["gateup"]
     # DRAM bytes per launch of k_gateup_tma at b = 1 (8 touched experts) from the committed ncu
-    # capture (profiles/decode_kernels_full_capture.md); only valid for that shape
-    traffic = 50.56e6 if (args.workload == "decode24" and b == 1) else None  # ncu, per launch
-    roof = {"bound": "hbm", "kernel": "k_gateup_tma (gate/up + SwiGLU, decode)",
+    # capture of the decode kernels; only valid for that shape and the bf16 kernel
+    traffic = (50.56e6 if (args.workload == "decode24" and b == 1 and not wl.get("fp4"))
+               else None)  # ncu, per launch
+    kname = "k_gateup_fp4" if wl.get("fp4") else "k_gateup_tma"
+    roof = {"bound": "hbm", "kernel": f"{kname} (gate/up + SwiGLU, decode)",
             "achieved": round(g["achieved"], 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
             "frac": round(g["achieved"] / pk["hbm_gbs"], 4), "traffic": traffic,
             "peak_source": pk["source"],
-            "algorithmic_bytes": "touched experts x 2*d_ff*d*2 B per call (50.33 MB at b=1)"}
+            "algorithmic_bytes": ("touched experts x 2*d_ff*d*17/32 B per call (MXFP4 codes "
+                                  "+ scales)" if wl.get("fp4") else
+                                  "touched experts x 2*d_ff*d*2 B per call (50.33 MB at b=1)")}
     line = {
         "metric": "MoE-layer tokens/s (decode trace, b=1"
+                  + (", MXFP4 experts" if wl.get("fp4") else "")
                   + (", frequency admission)" if wl.get("admission") else ")"),
         "value": round(res["tok_s_all"], 2), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(res["ms"] / args.steps, 4), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "mxfp4 weights, bf16 activations, fp32 accumulate" if wl.get("fp4") else "bf16",
+        "data": "synthetic",
         "config": {"workload": args.workload, "layers": wl["L"], "d": wl["d"],
                    "d_ff": wl["d_ff"], "experts": wl["E"], "top_k": wl["k"],
                    "n_slots": wl["n_slots"], "batch": b, "graph": True,
                    "admission": bool(wl.get("admission")),
-                   "l2": "inputs larger than L2 (every step streams >1.8 GB of experts)",
+                   "weights": "mxfp4" if wl.get("fp4") else "bf16",
+                   "l2": "inputs larger than L2 (every step streams "
+                         f">{wl['L'] * wl['k'] * entry_bytes(wl) / 1e9:.2f} GB of experts)",
                    "parallelism": f"replicas x{world}",
                    "per_batch": {str(bb): {k: (round(v, 4) if isinstance(v, float) else v)
                                            for k, v in r.items()
@@ -729,6 +755,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batches", default="", help="comma list of decode batch sizes")
     ap.add_argument("--slots", type=int, default=0, help="override the slot count")
+    ap.add_argument("--fp4", action="store_true",
+                    help="MXFP4 expert entries (decode workloads only)")
     ap.add_argument("--admission", action="store_true",
                     help="frequency admission: misses that would displace a more frequently "
                          "used entry are staged for one call instead of cached")
@@ -747,6 +775,8 @@ def main():
         wl["n_slots"] = args.slots
     if args.admission:
         wl["admission"] = 1
+    if args.fp4:
+        wl["fp4"] = 1
     if args.experts:
         wl["E"] = args.experts
     if args.layers:

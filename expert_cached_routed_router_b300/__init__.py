@@ -31,6 +31,8 @@ EXPORTS = [
     "ft_moe_get_dims", "ft_moe_profile", "ft_moe_profile_read", "ft_route_topk_noalloc",
 ]
 
+FT_WEIGHTS_BF16, FT_WEIGHTS_MXFP4 = 0, 1
+
 PROF_CLASSES = ["router", "topk", "control", "fill", "gateup", "down", "other"]
 
 
@@ -43,7 +45,8 @@ class FtError(RuntimeError):
 class ft_moe_opts(ctypes.Structure):
     _fields_ = [("n_shared", ctypes.c_int), ("prewarm", ctypes.c_int),
                 ("max_tokens", ctypes.c_int), ("debug_checks", ctypes.c_int),
-                ("prefill_topup", ctypes.c_int), ("admission", ctypes.c_int)]
+                ("prefill_topup", ctypes.c_int), ("admission", ctypes.c_int),
+                ("weight_format", ctypes.c_int)]
 
 
 class ft_cache_stats_t(ctypes.Structure):
@@ -141,9 +144,10 @@ def _stream(stream) -> int | None:
 # -------- functions with the C names (marshalling only) ----------------------------------
 
 def ft_moe_create(L, E, k, d, d_ff, n_slots, n_shared=0, prewarm=1, max_tokens=4096,
-                  debug_checks=0, prefill_topup=0, admission=0) -> int:
+                  debug_checks=0, prefill_topup=0, admission=0, weight_format=0) -> int:
     lib = load_library()
-    opts = ft_moe_opts(n_shared, prewarm, max_tokens, debug_checks, prefill_topup, admission)
+    opts = ft_moe_opts(n_shared, prewarm, max_tokens, debug_checks, prefill_topup, admission,
+                       weight_format)
     h = ctypes.c_void_p()
     _check(lib.ft_moe_create(L, E, k, d, d_ff, n_slots, ctypes.byref(opts), ctypes.byref(h)))
     return h.value
@@ -296,12 +300,13 @@ class MoELayerStack:
     """One ft_moe handle: L routed-MoE layers sharing one LRU expert-slot cache."""
 
     def __init__(self, L, E, k, d, d_ff, n_slots, n_shared=0, prewarm=1, max_tokens=4096,
-                 debug_checks=0, prefill_topup=0, admission=0):
+                 debug_checks=0, prefill_topup=0, admission=0, weight_format=0):
         self.L, self.E, self.k, self.d, self.d_ff = L, E, k, d, d_ff
         self.n_shared = n_shared
         self.entry_elems = 3 * d * d_ff
+        self.weight_format = weight_format
         self.h = ft_moe_create(L, E, k, d, d_ff, n_slots, n_shared, prewarm, max_tokens,
-                               debug_checks, prefill_topup, admission)
+                               debug_checks, prefill_topup, admission, weight_format)
 
     def close(self):
         if self.h:

@@ -405,6 +405,300 @@ __global__ void __launch_bounds__(kGemvThreads, 1) k_down_tma(
   if (!ok) set_status(ctr, FT_ERR_TIMEOUT);
 }
 
+// ---------------------------------------------------------------------------------------
+// MXFP4 entries (decode).  Codes Wg | Wu | Wd, then scales Wg | Wu | Wd; a row of K inputs
+// has K/2 code bytes (input 2i in the low nibble of byte i) and K/32 scale bytes.  A 16-byte
+// chunk of a row's codes is exactly one 32-input scale block, so lane work is per block:
+// the block's E2M1 values are dotted with the inputs, then the sum is multiplied by the
+// block's power-of-two scale (exact).
+// ---------------------------------------------------------------------------------------
+
+// E2M1 code (low 4 bits of c) -> fp32: the sign goes to bit 31 and the three magnitude bits
+// (2 exponent, 1 mantissa) to bits 22..24, which is the value times 2^-126 (a subnormal when
+// the exponent field is 0); one exact multiply by 2^126 restores it.  Relies on fp32
+// subnormals being kept (no flush-to-zero build flags).
+__device__ __forceinline__ float e2m1_f32(uint32_t c) {
+  return __uint_as_float(((c & 8u) << 28) | ((c & 7u) << 22)) * 0x1p126f;
+}
+
+// E8M0 scale byte -> 2^(s - 127); s = 255 is NaN.
+__device__ __forceinline__ float e8m0_f32(uint32_t s) {
+  return s == 0 ? __uint_as_float(0x00400000u)
+                : (s == 255 ? __uint_as_float(0x7FC00000u) : __uint_as_float(s << 23));
+}
+
+// The 8 inputs held by one 32-bit code word, in input order.
+__device__ __forceinline__ void decode8(uint32_t w, float (&v)[8]) {
+#pragma unroll
+  for (int e = 0; e < 8; ++e) v[e] = e2m1_f32(w >> (4 * e));
+}
+
+// acc + sum_e v[e] * x[e] over 8 bf16 inputs x (one uint4), in input order.
+__device__ __forceinline__ float dot8_vals(const float (&v)[8], uint4 xv, float acc) {
+  const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    acc = fmaf(v[2 * i], __uint_as_float(xw[i] << 16), acc);
+    acc = fmaf(v[2 * i + 1], __uint_as_float(xw[i] & 0xFFFF0000u), acc);
+  }
+  return acc;
+}
+
+template <int G, bool XS>
+__device__ __forceinline__ void gateup_rows_fp4(const uint4 *__restrict__ g,
+                                                const uint4 *__restrict__ uu,
+                                                const uint8_t *__restrict__ sg,
+                                                const uint8_t *__restrict__ su,
+                                                const uint4 *__restrict__ xs, const int32_t *tk,
+                                                int n, int nchunk, int nblk, int lane,
+                                                float (&ag)[G], float (&au)[G]) {
+  int row[G];
+#pragma unroll
+  for (int t = 0; t < G; ++t) {
+    ag[t] = au[t] = 0.f;
+    row[t] = (t < n) ? tk[t] * nchunk : 0;
+  }
+  for (int ch = lane; ch < nblk; ch += 32) {
+    const uint4 qg = g[ch], qu = uu[ch];
+    const uint32_t wg[4] = {qg.x, qg.y, qg.z, qg.w}, wu[4] = {qu.x, qu.y, qu.z, qu.w};
+    float bg[G], bu[G];
+#pragma unroll
+    for (int t = 0; t < G; ++t) bg[t] = bu[t] = 0.f;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      float vg[8], vu[8];
+      decode8(wg[q], vg);
+      decode8(wu[q], vu);
+#pragma unroll
+      for (int t = 0; t < G; ++t) {
+        if (t < n) {
+          const int xi = row[t] + 4 * ch + q;
+          const uint4 xv = XS ? xs[xi] : __ldg(xs + xi);
+          bg[t] = dot8_vals(vg, xv, bg[t]);
+          bu[t] = dot8_vals(vu, xv, bu[t]);
+        }
+      }
+    }
+    const float scg = e8m0_f32(sg[ch]), scu = e8m0_f32(su[ch]);
+#pragma unroll
+    for (int t = 0; t < G; ++t) {
+      ag[t] = fmaf(bg[t], scg, ag[t]);
+      au[t] = fmaf(bu[t], scu, au[t]);
+    }
+  }
+#pragma unroll
+  for (int t = 0; t < G; ++t) {
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) {
+      ag[t] += __shfl_xor_sync(0xffffffffu, ag[t], off);
+      au[t] += __shfl_xor_sync(0xffffffffu, au[t], off);
+    }
+  }
+}
+
+// gate/up + SwiGLU on MXFP4 entries.  Task = (item u, rows j0 .. j0+R-1; d_ff % R == 0);
+// stage = [R gate code rows | R up code rows | R gate scale rows | R up scale rows].
+template <bool XS>
+__global__ void __launch_bounds__(kGemvThreads, 1) k_gateup_fp4(
+    const WorkItem *__restrict__ work, DevCounters *__restrict__ ctr,
+    const uint16_t *__restrict__ x, const int32_t *__restrict__ tok, uint16_t *__restrict__ h,
+    int T, int d, int d_ff, int R, uint32_t stage_bytes, uint32_t ring_bytes) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  pdl_trigger();
+  const int nchunk = d >> 3, nblk = d >> 5;
+  const size_t cb = (size_t)d / 2, sbr = (size_t)d / 32;  // code / scale bytes of a row
+  const size_t x_bytes = XS ? (size_t)T * d * 2 : 0;
+  RingSmem r = ring_layout(smem, x_bytes, stage_bytes, ring_bytes);
+  const uint4 *xs = XS ? reinterpret_cast<const uint4 *>(smem) : reinterpret_cast<const uint4 *>(x);
+  ring_init(r);
+  pdl_wait();  // work list, fills and slot table from the kernels before; x may be too
+  if (XS)
+    for (int i = threadIdx.x; i < T * nchunk; i += blockDim.x)
+      reinterpret_cast<uint4 *>(smem)[i] = __ldg(reinterpret_cast<const uint4 *>(x) + i);
+  __syncthreads();
+  if (ctr->call_status != 0) return;
+  const int n_work = ctr->n_work;
+  const int n_jb = d_ff / R;
+  const long n_tasks = (long)n_work * n_jb;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const size_t scale0 = (size_t)3 * d * d_ff / 2;  // start of the scale region
+  bool ok = true;
+  if (warp == kGemvWarps) {
+    if (lane == 0) {
+      int cu = -1;
+      const uint8_t *W = nullptr;
+      ok = ring_produce(r, n_tasks, [&](long task, uint8_t *st, uint64_t *bar) {
+        const int u = (int)(task / n_jb), j0 = (int)(task - (long)u * n_jb) * R;
+        if (u != cu) {
+          cu = u;
+          W = reinterpret_cast<const uint8_t *>(work[u].W);
+        }
+        const uint32_t c_bytes = (uint32_t)(R * cb), s_bytes = (uint32_t)(R * sbr);
+        mbar_arrive_expect_tx(bar, 2 * c_bytes + 2 * s_bytes);
+        bulk_g2s(st, W + (size_t)j0 * cb, c_bytes, bar);
+        bulk_g2s(st + c_bytes, W + (size_t)d_ff * cb + (size_t)j0 * cb, c_bytes, bar);
+        bulk_g2s(st + 2 * c_bytes, W + scale0 + (size_t)j0 * sbr, s_bytes, bar);
+        bulk_g2s(st + 2 * c_bytes + s_bytes, W + scale0 + (size_t)d_ff * sbr + (size_t)j0 * sbr,
+                 s_bytes, bar);
+      });
+    }
+  } else {
+    int cu = -1;
+    WorkItem wi{};
+    ok = ring_consume(r, n_tasks, [&](long task, const uint8_t *st) {
+      const int u = (int)(task / n_jb), j0 = (int)(task - (long)u * n_jb) * R;
+      if (u != cu) {
+        cu = u;
+        wi = work[u];
+      }
+      const int c = wi.count;
+      for (int rr = 0; rr < R; ++rr) {
+        const uint4 *g = reinterpret_cast<const uint4 *>(st + rr * cb);
+        const uint4 *uu = reinterpret_cast<const uint4 *>(st + (R + rr) * cb);
+        const uint8_t *sg = st + 2 * R * cb + rr * sbr;
+        const uint8_t *su = st + 2 * R * cb + (R + rr) * sbr;
+        for (int t0 = 0; t0 < c; t0 += 4) {
+          const int n = min(4, c - t0);
+          const int32_t *tk = tok + wi.q0 + t0;
+          uint16_t *hq = h + (size_t)(wi.q0 + t0) * d_ff + j0 + rr;
+          if (n == 1) {
+            float ag[1], au[1];
+            gateup_rows_fp4<1, XS>(g, uu, sg, su, xs, tk, 1, nchunk, nblk, lane, ag, au);
+            if (lane == 0) hq[0] = f32_to_bf16(silu_mul(ag[0], au[0]));
+          } else {
+            float ag[4], au[4];
+            gateup_rows_fp4<4, XS>(g, uu, sg, su, xs, tk, n, nchunk, nblk, lane, ag, au);
+#pragma unroll
+            for (int t = 0; t < 4; ++t)
+              if (lane == t && t < n) hq[(size_t)t * d_ff] = f32_to_bf16(silu_mul(ag[t], au[t]));
+          }
+        }
+      }
+    });
+  }
+  if (!ok) set_status(ctr, FT_ERR_TIMEOUT);
+}
+
+template <int G>
+__device__ __forceinline__ void down_rows_fp4(const uint8_t *__restrict__ st, int R,
+                                              const uint16_t *__restrict__ hq, int n, int d_ff,
+                                              int lane, float (&part)[kDownRows][G]) {
+  const int nblk = d_ff >> 5;
+  const size_t cb = (size_t)d_ff / 2, sbr = (size_t)d_ff / 32;
+#pragma unroll
+  for (int r = 0; r < kDownRows; ++r)
+#pragma unroll
+    for (int t = 0; t < G; ++t) part[r][t] = 0.f;
+  for (int ch = lane; ch < nblk; ch += 32) {
+    uint4 hv[G][4];
+#pragma unroll
+    for (int t = 0; t < G; ++t)
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        hv[t][q] = (t < n) ? __ldg(reinterpret_cast<const uint4 *>(hq + (size_t)t * d_ff) + 4 * ch + q)
+                           : make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int r = 0; r < kDownRows; ++r) {
+      if (r < R) {
+        const uint4 qr = reinterpret_cast<const uint4 *>(st + r * cb)[ch];
+        const uint32_t w[4] = {qr.x, qr.y, qr.z, qr.w};
+        float b[G];
+#pragma unroll
+        for (int t = 0; t < G; ++t) b[t] = 0.f;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          float v[8];
+          decode8(w[q], v);
+#pragma unroll
+          for (int t = 0; t < G; ++t) b[t] = dot8_vals(v, hv[t][q], b[t]);
+        }
+        const float sc = e8m0_f32(st[R * cb + r * sbr + ch]);
+#pragma unroll
+        for (int t = 0; t < G; ++t) part[r][t] = fmaf(b[t], sc, part[r][t]);
+      }
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < kDownRows; ++r)
+#pragma unroll
+    for (int t = 0; t < G; ++t)
+#pragma unroll
+      for (int off = 16; off >= 1; off >>= 1)
+        part[r][t] += __shfl_xor_sync(0xffffffffu, part[r][t], off);
+}
+
+// down on MXFP4 entries: task = (item u, rows i0 .. i0+R-1 of W_down; d % R == 0, R <= 8);
+// stage = [R code rows | R scale rows].
+__global__ void __launch_bounds__(kGemvThreads, 1) k_down_fp4(
+    const WorkItem *__restrict__ work, DevCounters *__restrict__ ctr,
+    const uint16_t *__restrict__ h, float *__restrict__ y, int d, int d_ff, int R,
+    uint32_t stage_bytes, uint32_t ring_bytes) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  pdl_trigger();
+  const size_t cb = (size_t)d_ff / 2, sbr = (size_t)d_ff / 32;
+  RingSmem r = ring_layout(smem, 0, stage_bytes, ring_bytes);
+  ring_init(r);
+  __syncthreads();
+  pdl_wait();  // h comes from the gate/up kernel
+  if (ctr->call_status != 0) return;
+  const int n_work = ctr->n_work;
+  const int n_ib = d / R;
+  const long n_tasks = (long)n_work * n_ib;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const size_t codes_d = (size_t)d * d_ff;                       // 2 * d_ff * d/2
+  const size_t scales_d = (size_t)3 * d * d_ff / 2 + (size_t)2 * d_ff * (d / 32);
+  bool ok = true;
+  if (warp == kGemvWarps) {
+    if (lane == 0) {
+      int cu = -1;
+      const uint8_t *W = nullptr;
+      ok = ring_produce(r, n_tasks, [&](long task, uint8_t *st, uint64_t *bar) {
+        const int u = (int)(task / n_ib), i0 = (int)(task - (long)u * n_ib) * R;
+        if (u != cu) {
+          cu = u;
+          W = reinterpret_cast<const uint8_t *>(work[u].W);
+        }
+        const uint32_t c_bytes = (uint32_t)(R * cb), s_bytes = (uint32_t)(R * sbr);
+        mbar_arrive_expect_tx(bar, c_bytes + s_bytes);
+        bulk_g2s(st, W + codes_d + (size_t)i0 * cb, c_bytes, bar);
+        bulk_g2s(st + c_bytes, W + scales_d + (size_t)i0 * sbr, s_bytes, bar);
+      });
+    }
+  } else {
+    int cu = -1;
+    WorkItem wi{};
+    ok = ring_consume(r, n_tasks, [&](long task, const uint8_t *st) {
+      const int u = (int)(task / n_ib), i0 = (int)(task - (long)u * n_ib) * R;
+      if (u != cu) {
+        cu = u;
+        wi = work[u];
+      }
+      const int c = wi.count;
+      for (int t0 = 0; t0 < c; t0 += 4) {
+        const int n = min(4, c - t0);
+        const uint16_t *hq = h + (size_t)(wi.q0 + t0) * d_ff;
+        float *yq = y + (size_t)(wi.q0 + t0) * d + i0;
+        if (n == 1) {
+          float part[kDownRows][1];
+          down_rows_fp4<1>(st, R, hq, 1, d_ff, lane, part);
+#pragma unroll
+          for (int rr = 0; rr < kDownRows; ++rr)
+            if (lane == rr && rr < R) yq[rr] = part[rr][0];
+        } else {
+          float part[kDownRows][4];
+          down_rows_fp4<4>(st, R, hq, n, d_ff, lane, part);
+#pragma unroll
+          for (int rr = 0; rr < kDownRows; ++rr)
+#pragma unroll
+            for (int t = 0; t < 4; ++t)
+              if (lane == rr * 4 + t && rr < R && t < n) yq[(size_t)t * d + rr] = part[rr][t];
+        }
+      }
+    });
+  }
+  if (!ok) set_status(ctr, FT_ERR_TIMEOUT);
+}
+
 static int sm_count() {
   static int n = 0;
   if (!n) {
@@ -428,9 +722,53 @@ static void allow_smem(K kern, size_t smem) {
   }
 }
 
+// MXFP4: R rows per task from {16, 8, 4} with R*d a multiple of 512 (every scale copy then
+// starts and ends on a 16-byte boundary) and d_ff % R == 0 (no ragged task); 8 stages fit.
+static void launch_gateup_fp4(const WorkItem *work, DevCounters *ctr, const uint16_t *x,
+                              const int32_t *tok, uint16_t *h, int T, int d, int d_ff,
+                              cudaStream_t s) {
+  const uint32_t unit = (uint32_t)d * 17 / 16;  // code + scale bytes of one gate/up row pair
+  const size_t xb = (size_t)T * d * 2, xr = (xb + 127) & ~(size_t)127;
+  const bool xs = xr + (size_t)kGemvWarps * 4 * unit <= (224u << 10);
+  const uint32_t ring = xs ? (uint32_t)std::min<size_t>(kRingBytes, (224u << 10) - xr) : kRingBytes;
+  int R = 4;
+  for (int c : {16, 8})
+    if (d_ff % c == 0 && (c * d) % 512 == 0 && (size_t)kGemvWarps * c * unit <= ring) {
+      R = c;
+      break;
+    }
+  const uint32_t sb = (uint32_t)R * unit;
+  const size_t smem = ring_smem_bytes(xs ? xb : 0, sb, ring);
+  auto go = [&](auto kern) {
+    allow_smem(kern, smem);
+    launch_pdl(kern, dim3(sm_count()), dim3(kGemvThreads), smem, s, work, ctr, x, tok, h, T, d,
+               d_ff, R, sb, ring);
+  };
+  if (xs)
+    go(k_gateup_fp4<true>);
+  else
+    go(k_gateup_fp4<false>);
+}
+
+static void launch_down_fp4(const WorkItem *work, DevCounters *ctr, const uint16_t *h, float *y,
+                            int d, int d_ff, cudaStream_t s) {
+  const uint32_t unit = (uint32_t)d_ff * 17 / 32;  // code + scale bytes of one W_down row
+  const int R = ((size_t)kGemvWarps * kDownRows * unit <= kRingBytes) ? kDownRows : 4;
+  const uint32_t sb = (uint32_t)R * unit;
+  const size_t smem = ring_smem_bytes(0, sb, kRingBytes);
+  allow_smem(k_down_fp4, smem);
+  launch_pdl(k_down_fp4, dim3(sm_count()), dim3(kGemvThreads), smem, s, work, ctr, h, y, d, d_ff,
+             R, sb, kRingBytes);
+}
+
 void launch_gateup_gemv(const WorkItem *work, DevCounters *ctr, int max_work, const uint16_t *x,
-                        const int32_t *tok, uint16_t *h, int T, int d, int d_ff, cudaStream_t s) {
+                        const int32_t *tok, uint16_t *h, int T, int d, int d_ff, bool fp4,
+                        cudaStream_t s) {
   (void)max_work;
+  if (fp4) {
+    launch_gateup_fp4(work, ctr, x, tok, h, T, d, d_ff, s);
+    return;
+  }
   // one stage per consumer warp holding R gate+up row pairs (R <= 4), as many as fit next to
   // x (kept in shared memory when a one-pair stage per warp still fits in 224 KB)
   const uint32_t unit = 4u * d;
@@ -520,9 +858,13 @@ __global__ void k_combine(const float *__restrict__ y, const float *__restrict__
 }
 
 void launch_down_gemv(const WorkItem *work, DevCounters *ctr, int max_work, const uint16_t *h,
-                      float *y, int T, int d, int d_ff, cudaStream_t s) {
+                      float *y, int T, int d, int d_ff, bool fp4, cudaStream_t s) {
   (void)T;
   (void)max_work;
+  if (fp4) {
+    launch_down_fp4(work, ctr, h, y, d, d_ff, s);
+    return;
+  }
   const uint32_t unit = 2u * d_ff;
   const int R = std::max(1, std::min({d, kDownRows, (int)(kRingBytes / kGemvWarps / unit)}));
   const uint32_t sb = (uint32_t)R * unit;

@@ -100,6 +100,7 @@ struct ft_moe {
   int last_prefill_layers = 0;
   int prefill_topup = 0;
   int admission = 0;          // frequency admission (see ft_moe_opts)
+  bool fp4 = false;           // MXFP4 entries (decode calls only)
   int n_stage = 0;            // staging entries after the slots: E with admission, else 0
   uint32_t *freq = nullptr;   // admission counts [L][E]
   uint64_t last_h2d_bytes = 0, last_d2d_bytes = 0;  // moved by the last prefill
@@ -313,11 +314,12 @@ void experts_layer(ft_moe *h, const uint16_t *x, int T, uint16_t *out, const TcM
   if (T <= kGemvMaxTokens) {
     {
       ProfScope p(h, FT_PROF_GATEUP, s);
-      launch_gateup_gemv(h->work, h->ctr, max_work, x, h->tok, h->hbuf, T, h->d, h->d_ff, s);
+      launch_gateup_gemv(h->work, h->ctr, max_work, x, h->tok, h->hbuf, T, h->d, h->d_ff, h->fp4,
+                         s);
     }
     {
       ProfScope p(h, FT_PROF_DOWN, s);
-      launch_down_gemv(h->work, h->ctr, max_work, h->hbuf, h->ybuf, T, h->d, h->d_ff, s);
+      launch_down_gemv(h->work, h->ctr, max_work, h->hbuf, h->ybuf, T, h->d, h->d_ff, h->fp4, s);
     }
     ProfScope p(h, FT_PROF_OTHER, s);
     launch_combine(h->ybuf, h->w, h->inv, h->ctr, out, T, h->k, h->d, h->n_shared, s);
@@ -361,11 +363,15 @@ int ft_moe_create(int L, int E, int k, int d, int d_ff, int n_slots, const ft_mo
                 "need d in [128, 4096] and d_ff in [128, 8192], multiples of 128 (got %d, %d)", d,
                 d_ff);
   if (n_slots < 1) return fail(FT_ERR_INVALID, "n_slots must be >= 1 (got %d)", n_slots);
-  ft_moe_opts o{0, 1, 4096, 0, 0, 0};
+  ft_moe_opts o{0, 1, 4096, 0, 0, 0, FT_WEIGHTS_BF16};
   if (opts) o = *opts;
   if (o.max_tokens < 1 || o.max_tokens > (1 << 20))
     return fail(FT_ERR_INVALID, "max_tokens out of range (%d)", o.max_tokens);
   if (o.n_shared != 0 && o.n_shared != 1) return fail(FT_ERR_INVALID, "n_shared must be 0 or 1");
+  if (o.weight_format != FT_WEIGHTS_BF16 && o.weight_format != FT_WEIGHTS_MXFP4)
+    return fail(FT_ERR_INVALID, "unknown weight_format %d", o.weight_format);
+  if (o.weight_format == FT_WEIGHTS_MXFP4 && o.n_shared)
+    return fail(FT_ERR_INVALID, "MXFP4 entries: n_shared must be 0");
 
   ft_moe *h = new ft_moe();
   h->L = L;
@@ -381,8 +387,10 @@ int ft_moe_create(int L, int E, int k, int d, int d_ff, int n_slots, const ft_mo
   h->prefill_topup = o.prefill_topup != 0;
   h->admission = o.admission != 0;
   h->n_stage = h->admission ? E : 0;
-  h->entry_elems = (size_t)3 * d * d_ff;
-  h->entry_bytes = h->entry_elems * 2;
+  h->fp4 = o.weight_format == FT_WEIGHTS_MXFP4;
+  // entry_elems counts 16-bit units (pointer arithmetic on uint16_t), whatever the format
+  h->entry_bytes = h->fp4 ? (size_t)3 * d * d_ff * 17 / 32 : (size_t)3 * d * d_ff * 2;
+  h->entry_elems = h->entry_bytes / 2;
   h->has_bias.assign(L, 0);
   cudaGetDevice(&h->device);
 
@@ -440,7 +448,7 @@ int ft_moe_create(int L, int E, int k, int d, int d_ff, int n_slots, const ft_mo
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (e != cudaSuccess) rc = fail(FT_ERR_CUDA, "initialisation: %s", cudaGetErrorString(e));
   }
-  if (rc == FT_OK) rc = build_maps(h, &h->maps_slots, h->slots, n_slots + h->n_stage);
+  if (rc == FT_OK && !h->fp4) rc = build_maps(h, &h->maps_slots, h->slots, n_slots + h->n_stage);
   if (rc == FT_OK) rc = upload_cache_desc(h);
   if (rc != FT_OK) {
     free_all(h);
@@ -569,6 +577,9 @@ int ft_moe_forward(ft_moe *h, int layer, const void *x, int T, void *out, ft_str
   if (!x || !out) return fail(FT_ERR_INVALID, "x or out is NULL");
   if ((((uintptr_t)x) | ((uintptr_t)out)) & 15)
     return fail(FT_ERR_INVALID, "x and out must be 16-byte aligned");
+  if (h->fp4 && T > kGemvMaxTokens)
+    return fail(FT_ERR_INVALID, "MXFP4 entries: decode calls only (T <= %d, got %d)",
+                kGemvMaxTokens, T);
   cudaStream_t s = (cudaStream_t)stream;
   const uint16_t *xb = static_cast<const uint16_t *>(x);
   route_layer(h, layer, xb, T, true, nullptr, s);
@@ -625,6 +636,7 @@ int ft_moe_prefill_stream(ft_moe *h, int layer0, int n_layers, const void *x, in
                           ft_stream_t stream) {
   if (int r = check_handle(h)) return r;
   if (!h->pool_host) return fail(FT_ERR_STATE, "prefill before ft_moe_load_pool");
+  if (h->fp4) return fail(FT_ERR_INVALID, "MXFP4 entries: prefill is not supported");
   if (n_layers < 1 || layer0 < 0 || layer0 + n_layers > h->L)
     return fail(FT_ERR_INVALID, "layers [%d, %d) out of range", layer0, layer0 + n_layers);
   if (T < 1 || T > h->max_tokens)
@@ -816,7 +828,8 @@ int ft_cache_resize(ft_moe *h, int n_new) {
   h->stamps = nstamps;
   h->n_slots = n_new;
   if (int r = upload_cache_desc(h)) return r;
-  if (int r = build_maps(h, &h->maps_slots, h->slots, n_new + h->n_stage)) return r;
+  if (!h->fp4)
+    if (int r = build_maps(h, &h->maps_slots, h->slots, n_new + h->n_stage)) return r;
   DevCounters c{};
   FT_CUDA(cudaMemcpy(&c, h->ctr, sizeof(c), cudaMemcpyDeviceToHost));
   c.occupied = m;

@@ -36,10 +36,12 @@ void launch_fill(const uint16_t *pool_dev, const CacheDesc *cache, const int32_t
 
 // Decode expert FFN (T <= kGemvMaxTokens): gate/up GEMV + SwiGLU into h; down GEMV into the
 // fp32 per-row buffer y [(T*k + T)][d]; then the deterministic weighted combine into out.
+// fp4: the entries are MXFP4 (codes then block scales) instead of bf16
 void launch_gateup_gemv(const WorkItem *work, DevCounters *ctr, int max_work, const uint16_t *x,
-                        const int32_t *tok, uint16_t *h, int T, int d, int d_ff, cudaStream_t s);
+                        const int32_t *tok, uint16_t *h, int T, int d, int d_ff, bool fp4,
+                        cudaStream_t s);
 void launch_down_gemv(const WorkItem *work, DevCounters *ctr, int max_work, const uint16_t *h,
-                      float *y, int T, int d, int d_ff, cudaStream_t s);
+                      float *y, int T, int d, int d_ff, bool fp4, cudaStream_t s);
 void launch_combine(const float *y, const float *w, const int32_t *inv, const DevCounters *ctr,
                     uint16_t *out, int T, int k, int d, int shared, cudaStream_t s);
 

@@ -1,6 +1,7 @@
 """GPU side of the seeded input generator (``synth.cu``): fills large pools fast.
 
-Produces exactly the values of ``ft_synth.expert_entry`` / ``ft_synth.normal_bf16``.
+Produces exactly the values of ``ft_synth.expert_entry`` / ``ft_synth.normal_bf16`` and the
+bytes of ``ft_synth.expert_entry_fp4``.
 """
 from __future__ import annotations
 
@@ -10,7 +11,7 @@ import subprocess
 
 import numpy as np
 
-from . import TAG_POOL, TAG_X, ENTRY_SIGMA, stream_key
+from . import TAG_POOL, TAG_POOL_FP4, TAG_X, ENTRY_SIGMA, stream_key
 
 _DIR = os.path.dirname(os.path.abspath(__file__))
 LIB = os.path.join(_DIR, "libft_synth.so")
@@ -41,6 +42,9 @@ def _load():
                                              ctypes.c_uint64, ctypes.c_uint64, ctypes.c_float,
                                              ctypes.c_void_p, ctypes.c_void_p]
         _lib.fts_generate_device.restype = ctypes.c_int
+        _lib.fts_fill_host_fp4.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_uint64,
+                                           ctypes.c_uint64, ctypes.c_void_p, ctypes.c_int]
+        _lib.fts_fill_host_fp4.restype = ctypes.c_int
     return _lib
 
 
@@ -53,6 +57,17 @@ def fill_pool(dst_host_ptr: int, seed: int, L: int, E: int, d: int, d_ff: int,
                                float(np.float32(ENTRY_SIGMA)), dst_host_ptr, stage_entries)
     if rc != 0:
         raise RuntimeError(f"fts_fill_host failed with CUDA error {rc}")
+
+
+def fill_pool_fp4(dst_host_ptr: int, seed: int, L: int, E: int, d: int, d_ff: int,
+                  stage_entries: int = 256):
+    """Write the [L][E][entry] pool of expert_entry_fp4(seed, l, e, d, d_ff) into host memory."""
+    keys = np.array([stream_key(seed, TAG_POOL_FP4, l, e) for l in range(L) for e in range(E)],
+                    dtype=np.uint64)
+    rc = _load().fts_fill_host_fp4(keys.ctypes.data, len(keys), 3 * d * d_ff // 2,
+                                   3 * d * d_ff // 32, dst_host_ptr, stage_entries)
+    if rc != 0:
+        raise RuntimeError(f"fts_fill_host_fp4 failed with CUDA error {rc}")
 
 
 def activations_device(dst_dev_ptr: int, seed: int, streams, T: int, d: int, stream=0):

@@ -47,9 +47,64 @@ __global__ void k_gen(const uint64_t *__restrict__ keys, int n_keys, uint64_t pe
   }
 }
 
+// 4-bit entries (ft_synth.expert_entry_fp4): entry k is `nc` code bytes (the little-endian
+// bytes of draws 0 .. nc/8 - 1 of keys[k]) then `ns` scale bytes (118 + draw(nc/8 + j) % 3).
+__global__ void k_gen_fp4(const uint64_t *__restrict__ keys, int n_keys, uint64_t nc,
+                          uint64_t ns, uint8_t *__restrict__ dst) {
+  const uint64_t per = nc + ns, nd = nc / 8, units = nd + ns;
+  const uint64_t total = (uint64_t)n_keys * units;
+  for (uint64_t t = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; t < total;
+       t += (uint64_t)gridDim.x * blockDim.x) {
+    const uint64_t k = t / units, i = t - k * units;
+    const uint64_t v = mix64(keys[k] + (i + 1) * kG);
+    if (i < nd)
+      *reinterpret_cast<uint64_t *>(dst + k * per + 8 * i) = v;  // little-endian bytes
+    else
+      dst[k * per + nc + (i - nd)] = (uint8_t)(118 + v % 3);
+  }
+}
+
 }  // namespace
 
 extern "C" {
+
+// Fill a host buffer with n_keys consecutive 4-bit entries (nc code bytes + ns scale bytes
+// each, nc a multiple of 16), staged through two device buffers like fts_fill_host.
+int fts_fill_host_fp4(const uint64_t *keys_host, int n_keys, uint64_t nc, uint64_t ns,
+                      void *dst_host, int stage_entries) {
+  if (n_keys <= 0) return 0;
+  if (stage_entries < 1) stage_entries = 1;
+  const uint64_t per = nc + ns;
+  cudaStream_t st[2];
+  uint8_t *buf[2] = {nullptr, nullptr};
+  uint64_t *dk = nullptr;
+  cudaError_t e = cudaSuccess;
+  for (int i = 0; i < 2 && e == cudaSuccess; ++i) e = cudaStreamCreate(&st[i]);
+  for (int i = 0; i < 2 && e == cudaSuccess; ++i)
+    e = cudaMalloc(&buf[i], (size_t)stage_entries * per);
+  if (e == cudaSuccess) e = cudaMalloc(&dk, (size_t)n_keys * 8);
+  if (e == cudaSuccess) e = cudaMemcpy(dk, keys_host, (size_t)n_keys * 8, cudaMemcpyHostToDevice);
+  for (int c = 0, it = 0; e == cudaSuccess && c < n_keys; c += stage_entries, ++it) {
+    const int b = it & 1;
+    const int m = (n_keys - c) < stage_entries ? (n_keys - c) : stage_entries;
+    k_gen_fp4<<<148 * 8, 256, 0, st[b]>>>(dk + c, m, nc, ns, buf[b]);
+    e = cudaGetLastError();
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(static_cast<uint8_t *>(dst_host) + (size_t)c * per, buf[b],
+                          (size_t)m * per, cudaMemcpyDeviceToHost, st[b]);
+  }
+  for (int i = 0; i < 2; ++i) {
+    cudaError_t e2 = cudaStreamSynchronize(st[i]);
+    if (e == cudaSuccess) e = e2;
+  }
+  for (int i = 0; i < 2; ++i) {
+    if (buf[i]) cudaFree(buf[i]);
+    cudaStreamDestroy(st[i]);
+  }
+  if (dk) cudaFree(dk);
+  return (int)e;
+}
+
 
 // Generate n_keys streams of `n` bf16 values each (elements start..start+n-1) into device
 // memory dst_dev, stream k at dst_dev + k * per_key.  Returns a cudaError_t value.

@@ -70,7 +70,24 @@ typedef struct {
   int admission;     /* [0] 1 = frequency admission: a miss that finds no free slot replaces
                             the next LRU victim only if its access count is at least the
                             victim's, else it is staged for the one call (see below)       */
+  int weight_format; /* [FT_WEIGHTS_BF16] expert entry format, see below                  */
 } ft_moe_opts;
+
+/*
+ * Expert entry formats (ft_moe_opts.weight_format).
+ *   FT_WEIGHTS_BF16:  Wg [d_ff][d] | Wu [d_ff][d] | Wd [d][d_ff], bf16, every row one output
+ *                     feature contiguous over its inputs; 6*d*d_ff bytes.
+ *   FT_WEIGHTS_MXFP4: the same matrices in MXFP4 - the format the pages deploy routed
+ *                     experts in (FreeToken benchmark, "benchmark results", model table),
+ *                     read as OCP Microscaling MXFP4: E2M1 codes, one E8M0 power-of-two
+ *                     scale per 32 inputs of a row.  Codes Wg [d_ff][d/2] | codes Wu
+ *                     [d_ff][d/2] | codes Wd [d][d_ff/2] | scales Wg [d_ff][d/32] | scales Wu
+ *                     [d_ff][d/32] | scales Wd [d][d_ff/32]; input 2i of a row is the low
+ *                     nibble of byte i, 2i+1 the high nibble; 3*d*d_ff*17/32 bytes.  Decode
+ *                     calls only: forward with T > 16 and prefill return FT_ERR_INVALID, and
+ *                     n_shared must be 0.
+ */
+enum { FT_WEIGHTS_BF16 = 0, FT_WEIGHTS_MXFP4 = 1 };
 
 /* Cache counters, accumulated on the device since creation or the last reset. */
 typedef struct {

@@ -9,17 +9,19 @@ from oracle import moe as omoe
 
 
 class Config:
-    def __init__(self, L, E, k, d, d_ff, n_slots, n_shared=0, seed=0):
+    def __init__(self, L, E, k, d, d_ff, n_slots, n_shared=0, seed=0, fp4=False):
         self.L, self.E, self.k, self.d, self.d_ff = L, E, k, d, d_ff
-        self.n_slots, self.n_shared, self.seed = n_slots, n_shared, seed
+        self.n_slots, self.n_shared, self.seed, self.fp4 = n_slots, n_shared, seed, fp4
         self.entry_elems = 3 * d * d_ff
-        self.entry_bytes = 2 * self.entry_elems
+        self.entry_bytes = (ft_synth.entry_bytes_fp4(d, d_ff) if fp4 else 2 * self.entry_elems)
         self._entries = {}
 
     def entry(self, l, e):
+        """bf16 bits (uint16), or the packed 4-bit entry (uint8) with fp4."""
         key = (l, e)
         if key not in self._entries:
-            self._entries[key] = ft_synth.expert_entry(self.seed, l, e, self.d, self.d_ff)
+            gen = ft_synth.expert_entry_fp4 if self.fp4 else ft_synth.expert_entry
+            self._entries[key] = gen(self.seed, l, e, self.d, self.d_ff)
         return self._entries[key]
 
     def shared(self, l):
@@ -30,14 +32,19 @@ class Config:
 
 
 def host_pool(cfg: Config):
-    """Pinned torch uint16-as-int16 tensor [L*E*entry] built from the generator."""
+    """Pinned torch tensor [L*E*entry] built from the generator (int16 for bf16 entries,
+    uint8 for 4-bit ones)."""
     import torch
-    pool = torch.empty(cfg.L * cfg.E * cfg.entry_elems, dtype=torch.int16, pin_memory=True)
-    view = pool.numpy().view(np.uint16)
+    if cfg.fp4:
+        pool = torch.empty(cfg.L * cfg.E * cfg.entry_bytes, dtype=torch.uint8, pin_memory=True)
+        view, n = pool.numpy(), cfg.entry_bytes
+    else:
+        pool = torch.empty(cfg.L * cfg.E * cfg.entry_elems, dtype=torch.int16, pin_memory=True)
+        view, n = pool.numpy().view(np.uint16), cfg.entry_elems
     for l in range(cfg.L):
         for e in range(cfg.E):
-            o = (l * cfg.E + e) * cfg.entry_elems
-            view[o:o + cfg.entry_elems] = cfg.entry(l, e)
+            o = (l * cfg.E + e) * n
+            view[o:o + n] = cfg.entry(l, e)
     return pool
 
 
@@ -46,8 +53,12 @@ def gpu_host_pool(cfg: Config):
     import torch
     import ft_synth.gpu as sg
     sg.build()
-    pool = torch.empty(cfg.L * cfg.E * cfg.entry_elems, dtype=torch.int16, pin_memory=True)
-    sg.fill_pool(pool.data_ptr(), cfg.seed, cfg.L, cfg.E, cfg.d, cfg.d_ff)
+    if cfg.fp4:
+        pool = torch.empty(cfg.L * cfg.E * cfg.entry_bytes, dtype=torch.uint8, pin_memory=True)
+        sg.fill_pool_fp4(pool.data_ptr(), cfg.seed, cfg.L, cfg.E, cfg.d, cfg.d_ff)
+    else:
+        pool = torch.empty(cfg.L * cfg.E * cfg.entry_elems, dtype=torch.int16, pin_memory=True)
+        sg.fill_pool(pool.data_ptr(), cfg.seed, cfg.L, cfg.E, cfg.d, cfg.d_ff)
     return pool
 
 
@@ -61,22 +72,25 @@ def make_stack(cfg: Config, max_tokens=512, prewarm=1, pool=None, **opts):
     import torch
     from expert_cached_routed_router_b300 import MoELayerStack
     st = MoELayerStack(cfg.L, cfg.E, cfg.k, cfg.d, cfg.d_ff, cfg.n_slots, n_shared=cfg.n_shared,
-                       prewarm=prewarm, max_tokens=max_tokens, **opts)
+                       prewarm=prewarm, max_tokens=max_tokens, weight_format=1 if cfg.fp4 else 0,
+                       **opts)
     for l in range(cfg.L):
         st.load_router(l, to_dev_bf16(cfg.router(l)))
         if cfg.n_shared:
             st.load_shared(l, to_dev_bf16(cfg.shared(l)))
     pool = host_pool(cfg) if pool is None else pool
-    st.load_pool(pool, pool.numel() * 2)
+    st.load_pool(pool, pool.numel() * pool.element_size())
     torch.cuda.synchronize()
     st._pool = pool     # keep alive
     return st
 
 
 def oracle_layer(cfg: Config, l, x_bits, bias=None, tokens=None):
+    from oracle import fp4 as ofp4
     return omoe.moe_layer(x_bits, cfg.router(l), cfg.k, lambda e: cfg.entry(l, e), cfg.d,
                           cfg.d_ff, bias=bias,
-                          shared_entry=cfg.shared(l) if cfg.n_shared else None, tokens=tokens)
+                          shared_entry=cfg.shared(l) if cfg.n_shared else None, tokens=tokens,
+                          ffn=ofp4.expert_ffn_fp4 if cfg.fp4 else None)
 
 
 def out_bits_to_f64(t):

@@ -51,6 +51,15 @@ def test_create_rejects_bad_shapes(args):
     assert ei.value.code == ftm.FT_ERR_INVALID
 
 
+def test_create_rejects_bad_weight_format():
+    with pytest.raises(ftm.FtError) as ei:
+        ftm.ft_moe_create(1, 16, 2, 256, 128, 16, weight_format=2)
+    assert ei.value.code == ftm.FT_ERR_INVALID
+    with pytest.raises(ftm.FtError) as ei:
+        ftm.ft_moe_create(1, 16, 2, 256, 128, 16, n_shared=1, weight_format=1)
+    assert ei.value.code == ftm.FT_ERR_INVALID
+
+
 def test_null_handle_is_rejected():
     lib = ftm.load_library()
     assert lib.ft_moe_forward(None, 0, None, 1, None, None) == ftm.FT_ERR_INVALID

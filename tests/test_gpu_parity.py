@@ -185,6 +185,52 @@ def test_admission_trace_bit_exact(T):
     st.close()
 
 
+@pytest.mark.parametrize("T,admission", [(1, 0), (4, 0), (16, 0), (4, 1)])
+def test_mxfp4_decode_trace(T, admission):
+    """MXFP4 entries: a drifting decode trace with evictions (fills move the 4-bit entries);
+    routing, fills and cache state bit-exact; outputs against the oracle's expert network on
+    the dequantized weights, within tolerance."""
+    import torch
+    cfg = Config(L=3, E=16, k=2, d=256, d_ff=384, n_slots=10, seed=14, fp4=True)
+    st = make_stack(cfg, max_tokens=16, admission=admission)
+    sim = olru.SlotCacheSim(cfg.L, cfg.E, cfg.n_slots, cfg.entry_bytes, prewarm=True,
+                            admission=bool(admission))
+    gen = ft_synth.DriftingZipfBias(14, cfg.L, cfg.E, s=1.0, sigma_walk=0.3)
+    for step in range(8):
+        gen.advance()
+        x = ft_synth.activations(14, 300 + step, T, cfg.d)
+        for l in range(cfg.L):
+            b = gen.bias(l)
+            st.set_router_bias(l, torch.from_numpy(b).cuda())
+            out = _run(st, l, x)
+            ref = oracle_layer(cfg, l, x, bias=b, tokens=np.arange(min(T, 4)))
+            assert_routing_equal(st, ref, T)
+            code, hits, fills = sim.access(l, ref["idx"].ravel())
+            assert code == olru.OK
+            np.testing.assert_array_equal(st.fills(), np.array([f[:3] for f in fills],
+                                                                dtype=np.int32).reshape(-1, 3))
+            assert_cache_equal(st, sim)
+            assert_out_close(out_bits_to_f64(out)[ref["tokens"]], ref["out"])
+    s = st.stats()
+    assert s["misses"] == sim.misses > 0 and s["status"] == 0
+    assert s["fill_bytes"] == sim.misses * cfg.entry_bytes
+    st.close()
+
+
+def test_mxfp4_refuses_grouped_gemm_and_prefill():
+    import torch
+    from expert_cached_routed_router_b300 import FtError
+    cfg = Config(L=1, E=16, k=2, d=256, d_ff=128, n_slots=16, seed=15, fp4=True)
+    st = make_stack(cfg, max_tokens=64)
+    x = to_dev_bf16(ft_synth.activations(15, 0, 17, cfg.d))
+    out = torch.empty_like(x)
+    with pytest.raises(FtError):
+        st.forward(0, x, out)
+    with pytest.raises(FtError):
+        st.prefill(0, 1, x, torch.empty((1, 17, cfg.d), dtype=torch.int16, device="cuda"))
+    st.close()
+
+
 def test_capacity_error_leaves_cache_unchanged():
     cfg = Config(L=1, E=16, k=4, d=256, d_ff=128, n_slots=3, seed=4)
     st = make_stack(cfg, max_tokens=16)
