@@ -217,6 +217,43 @@ def test_mxfp4_decode_trace(T, admission):
     st.close()
 
 
+@pytest.mark.parametrize("fp4", [False, True])
+def test_admission_across_resizes(fp4):
+    """Admission counts survive resizes (shrink, then grow past the start), with bf16 and
+    MXFP4 entries: fills, cache state and counters bit-exact against the oracle simulator."""
+    import torch
+    cfg = Config(L=3, E=16, k=2, d=256, d_ff=256, n_slots=12, seed=16, fp4=fp4)
+    st = make_stack(cfg, max_tokens=16, admission=1)
+    sim = olru.SlotCacheSim(cfg.L, cfg.E, cfg.n_slots, cfg.entry_bytes, prewarm=True,
+                            admission=True)
+    gen = ft_synth.DriftingZipfBias(16, cfg.L, cfg.E, s=1.1, sigma_walk=0.3)
+    resizes = {10: 5, 20: 30}
+    for step in range(30):
+        if step in resizes:
+            st.resize(resizes[step])
+            sim.resize(resizes[step])
+            assert_cache_equal(st, sim)
+        gen.advance()
+        x = ft_synth.activations(16, 700 + step, 4, cfg.d)
+        for l in range(cfg.L):
+            b = gen.bias(l)
+            st.set_router_bias(l, torch.from_numpy(b).cuda())
+            out = _run(st, l, x)
+            want = step % 10 == 9
+            ref = oracle_layer(cfg, l, x, bias=b, tokens=None if want else [])
+            code, hits, fills = sim.access(l, ref["idx"].ravel())
+            assert code == olru.OK
+            np.testing.assert_array_equal(st.fills(), np.array([f[:3] for f in fills],
+                                                                dtype=np.int32).reshape(-1, 3))
+            assert_cache_equal(st, sim)
+            if want:
+                assert_out_close(out_bits_to_f64(out), ref["out"])
+    s = st.stats()
+    assert s["bypasses"] == sim.bypasses > 0 and s["evictions"] == sim.evictions
+    assert s["status"] == 0 and s["resizes"] == 2
+    st.close()
+
+
 def test_mxfp4_refuses_grouped_gemm_and_prefill():
     import torch
     from expert_cached_routed_router_b300 import FtError
