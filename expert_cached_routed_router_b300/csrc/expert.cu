@@ -885,7 +885,9 @@ void launch_combine(const float *y, const float *w, const int32_t *inv, const De
 // Larger T: gather the permuted activation rows, grouped GEMMs, fp32 combine, cast.
 // ---------------------------------------------------------------------------------------
 __global__ void k_gather_rows(const uint16_t *__restrict__ x, const int32_t *__restrict__ tok,
-                              uint16_t *__restrict__ xp, int rows, int d) {
+                              uint16_t *__restrict__ xp, int rows, int d,
+                              const DevCounters *__restrict__ ctr) {
+  if (ctr->call_status != 0) return;  // refused call: tok is not this call's
   const int nchunk = d >> 3;
   const size_t n = (size_t)rows * nchunk;
   for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
@@ -897,12 +899,13 @@ __global__ void k_gather_rows(const uint16_t *__restrict__ x, const int32_t *__r
 }
 
 void launch_gather_rows(const uint16_t *x, const int32_t *tok, uint16_t *xp, int rows, int d,
+                        const DevCounters *ctr,
                         cudaStream_t s) {
   if (rows <= 0) return;
   const size_t n = (size_t)rows * (d >> 3);
   const int threads = 256;
   const unsigned blocks = (unsigned)std::min<size_t>((n + threads - 1) / threads, 148 * 16);
-  k_gather_rows<<<blocks, threads, 0, s>>>(x, tok, xp, rows, d);
+  k_gather_rows<<<blocks, threads, 0, s>>>(x, tok, xp, rows, d, ctr);
 }
 
 __global__ void k_cast_out(const float *__restrict__ acc, uint16_t *__restrict__ out, size_t n,

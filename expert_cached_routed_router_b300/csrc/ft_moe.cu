@@ -327,7 +327,7 @@ void experts_layer(ft_moe *h, const uint16_t *x, int T, uint16_t *out, const TcM
     const int rows = P + (h->n_shared ? T : 0);
     {
       ProfScope p(h, FT_PROF_OTHER, s);
-      launch_gather_rows(x, h->tok, h->xp, rows, h->d, s);
+      launch_gather_rows(x, h->tok, h->xp, rows, h->d, h->ctr, s);
       cudaMemsetAsync(h->acc, 0, (size_t)T * h->d * sizeof(float), s);
     }
     {

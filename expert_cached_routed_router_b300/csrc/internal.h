@@ -47,6 +47,7 @@ void launch_combine(const float *y, const float *w, const int32_t *inv, const De
 
 // Grouped-GEMM expert FFN for larger T.
 void launch_gather_rows(const uint16_t *x, const int32_t *tok, uint16_t *xp, int rows, int d,
+                        const DevCounters *ctr,
                         cudaStream_t s);
 void launch_cast_out(const float *acc, uint16_t *out, size_t n, const DevCounters *ctr,
                      cudaStream_t s);

@@ -351,7 +351,7 @@ constexpr unsigned long long kFieldMask = (1ull << kFieldBits) - 1;
 
 enum {
   kMiscNear = 0, kMiscDigit, kMiscNeed, kMiscCand, kMiscErr,
-  kMiscHalve, kMiscAdmit, kMiscEvict, kMiscBypass, kMiscN
+  kMiscHalve, kMiscAdmit, kMiscEvict, kMiscBypass, kMiscBad, kMiscN
 };
 
 struct CtlSmem {
@@ -420,6 +420,12 @@ __device__ __forceinline__ float topk_cta(const ControlArgs &a, const float *log
                                           CtlSmem &sm) {
   const int T = a.T, E = a.E, k = a.k, n = T * E, tid = threadIdx.x;
   for (int i = tid; i < n; i += 1024) sm.u.logit[i] = __ldcg(logits + i);
+  // a position no expert ranks into (NaN logits compare false) stays -1: an invalid pair
+  for (int p = tid; p < T * k; p += 1024) {
+    sm.pe[p] = -1;
+    sm.pv[p] = 0.f;
+  }
+  if (tid < kGemvMaxTokens) sm.next[tid] = 0.f;
   cta_sync();
   for (int i = tid; i < n; i += 1024) {
     const int t = i / E, e = i - t * E;
@@ -576,19 +582,38 @@ __device__ __forceinline__ void control_body(const ControlArgs &a, int mode,
   float my_w = 0.f;
   if (mode == 2) {
     my_w = topk_cta(a, logits, sm);
-    if (tid < P) atomicAdd(&sm.cnt[sm.pe[tid]], 1);
+    if (tid < P) {
+      const int e = sm.pe[tid];
+      if (e >= 0 && e < E)
+        atomicAdd(&sm.cnt[e], 1);
+      else
+        atomicAdd(&sm.misc[kMiscBad], 1);
+    }
   } else if (mode == 0) {
     for (int p = tid; p < P; p += 1024) {
       const int e = a.idx[p];
       if (e >= 0 && e < E)
         atomicAdd(&sm.cnt[e], 1);
       else
-        set_status(a.ctr, FT_ERR_INVALID);
+        atomicAdd(&sm.misc[kMiscBad], 1);
     }
   } else {
     for (int e = tid; e < E; e += 1024) sm.cnt[e] = a.counts[e];
+    // the multi-CTA grouping skips invalid pairs: then its counts do not add up to P
+    if (tid == 0 && a.offsets[E - 1] + a.counts[E - 1] != P) atomicAdd(&sm.misc[kMiscBad], 1);
   }
   cta_sync();
+  // an invalid pair (non-finite logits leave experts unranked) refuses the call like a
+  // capacity overflow: nothing downstream runs on a partial grouping
+  if (sm.misc[kMiscBad]) {
+    if (tid == 0) {
+      set_status(a.ctr, FT_ERR_INVALID);
+      a.ctr->call_status = FT_ERR_INVALID;
+      a.ctr->n_work = 0;
+      a.ctr->n_fill = 0;
+    }
+    return;
+  }
 
   // one scan over experts: offsets (modes 0, 2), hit / touched rank, miss rank
   const int cnt = tid < E ? sm.cnt[tid] : 0;

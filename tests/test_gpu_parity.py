@@ -424,6 +424,35 @@ def test_chained_layers_read_previous_output(T):
     st.close()
 
 
+@pytest.mark.parametrize("E,k,T", [(32, 4, 1), (512, 8, 16), (32, 4, 40), (32, 4, 300)])
+def test_non_finite_input_refuses_call(E, k, T):
+    """All-NaN activations leave every logit NaN, so no expert can be ranked: the call is
+    refused with FT_ERR_INVALID (in-CTA top-k, warp top-k, single- and multi-CTA grouping),
+    out is not written, the cache does not change, and the next valid call is exact."""
+    import torch
+    from expert_cached_routed_router_b300 import FT_ERR_INVALID
+    # room for the T*k distinct experts of the valid call that follows (128 at T = 16, k = 8)
+    cfg = Config(L=1, E=E, k=k, d=128, d_ff=128, n_slots=160, seed=17)
+    st = make_stack(cfg, max_tokens=512, pool=gpu_host_pool(cfg))
+    before = st.cache_state()
+    x = torch.full((T, cfg.d), 0x7FC0, dtype=torch.int16, device="cuda")   # bf16 NaN
+    out = torch.zeros_like(x)
+    st.forward(0, x, out)
+    torch.cuda.synchronize()
+    assert st.status() == FT_ERR_INVALID
+    assert int(out.abs().sum()) == 0
+    for a_, b_ in zip(before, st.cache_state()):
+        np.testing.assert_array_equal(a_, b_)
+    st.stats_reset()
+    xv = ft_synth.activations(17, T, T, cfg.d)
+    out = _run(st, 0, xv)
+    ref = oracle_layer(cfg, 0, xv, tokens=np.arange(min(T, 4)))
+    assert_routing_equal(st, ref, T)
+    assert_out_close(out_bits_to_f64(out)[ref["tokens"]], ref["out"])
+    assert st.status() == 0
+    st.close()
+
+
 def test_forward_is_deterministic():
     cfg = Config(L=1, E=32, k=4, d=512, d_ff=384, n_slots=32, seed=8)
     st = make_stack(cfg, max_tokens=16)
