@@ -162,7 +162,9 @@ int ft_moe_load_shared(ft_moe *h, int layer, const void *entry_bf16);
  * combine, all on `stream`, with no host synchronisation, so a sequence of calls can be
  * captured into a CUDA graph (for a fixed T).  If the call touches more distinct experts
  * than n_slots, the device status becomes FT_ERR_CAPACITY, the cache is unchanged and
- * out is left unwritten.  x and out may not overlap.
+ * out is left unwritten; a call whose logits leave some token without k rankable experts
+ * (non-finite activations) is refused the same way with FT_ERR_INVALID.  x and out may not
+ * overlap.
  */
 int ft_moe_forward(ft_moe *h, int layer, const void *x, int T, void *out, ft_stream_t stream);
 
