@@ -9,7 +9,10 @@ input generator ``ft_synth``.
   the permutation grouped by expert, the SwiGLU expert FFN and the weighted combine
   (fp64), and an independently written dense SwiGLU FFN for the 1-expert special case.
 * ``oracle.lru``  - the slot-level LRU cache simulator (slot table, owners, stamps, fills,
-  resize) and an independently written brute-force LRU used to pin it.
+  resize, optional frequency admission) and an independently written brute-force LRU used
+  to pin it.
+* ``oracle.fp4``  - MXFP4 entries: E2M1 codes and E8M0 block scales dequantized exactly, and
+  the SwiGLU expert on the dequantized weights.
 
 Sources.  The system is FreeToken as described on the freetoken.wiki pages
 "FreeToken RTX 4090" (section "how the MoE memory hierarchy works": complete
