@@ -51,6 +51,9 @@ WORKLOADS = {
                     steps=10000, phase=1000, resizes=((3500, 307), (6500, 1228))),
 }
 SEED = 0
+# DRAM bytes per launch of the decode expert kernel on an all-hit b=1 call of the 24-layer trace
+# (8 entries of 9.44 MB), from the committed ncu capture; None until that capture exists
+TRAFFIC_DECODE24_B1 = None
 
 
 def peaks():
@@ -298,11 +301,11 @@ def profile_decode_batch(wl, pool, b, x_all, bias_all, W, K, seed):
     st.profile_read()
     s0 = st.stats()
     from expert_cached_routed_router_b300 import PROF_CLASSES
-    prof = {c: (0.0, 0) for c in PROF_CLASSES}
+    prof = {c: (0.0, 0, 0) for c in PROF_CLASSES}
     for t in range(W, W + K):
         run(t)
         p = st.profile_read()
-        prof = {c: (prof[c][0] + p[c][0], prof[c][1] + p[c][1]) for c in PROF_CLASSES}
+        prof = {c: tuple(a + b for a, b in zip(prof[c], p[c])) for c in PROF_CLASSES}
     s1 = st.stats()
     st.profile(False)
     touched = (s1["hits"] - s0["hits"]) + (s1["misses"] - s0["misses"])
@@ -373,18 +376,46 @@ def cpu_oracle_decode(wl, pool, b, bias_np, seed, budget_s=15.0, max_calls=None)
         step += 1
 
 
-def roofline_decode(wl, prof, touched, n_calls, pk):
-    """Achieved HBM GB/s of the gate/up GEMV (the largest HBM consumer of the step)."""
-    d, d_ff = wl["d"], wl["d_ff"]
-    per_matrix = entry_bytes(wl) // 3                    # bytes of one d x d_ff matrix
-    gate_bytes = touched * 2 * per_matrix
-    down_bytes = touched * per_matrix
-    g_ms, g_n = prof["gateup"]
-    dn_ms, dn_n = prof["down"]
+def measure_h2d(nbytes=1 << 30, reps=5):
+    """Pinned host -> device cudaMemcpyAsync GB/s (best of ``reps``), in this run."""
+    import torch
+    src = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    dst = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    best = 0.0
+    for _ in range(reps + 1):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        dst.copy_(src, non_blocking=True)
+        e1.record()
+        torch.cuda.synchronize()
+        best = max(best, nbytes / (e0.elapsed_time(e1) / 1e3) / 1e9)
+    del src, dst
+    return best
+
+
+def roofline_decode(wl, prof, pk):
+    """HBM rooflines of the decode step from the per-launch record.
+
+    experts_hit: the decode expert kernel on calls without misses, HBM bound: bytes = the
+    entries it streams (touched experts + shared) x entry bytes.  experts_miss: the same kernel
+    on calls with misses, bound by the host link (its fills) with the hit experts overlapped.
+    step_m2: touched bytes (entries + router weights) over routing + expert-kernel time of the
+    calls without misses (the survey's decode metric with fills excluded)."""
+    eb = entry_bytes(wl)
+    router_bytes = wl["E"] * wl["d"] * 2
     out = {}
-    for name, byt, ms, n in (("gateup", gate_bytes, g_ms, g_n), ("down", down_bytes, dn_ms, dn_n)):
-        gbs = byt / (ms / 1e3) / 1e9 if ms > 0 else 0.0
-        out[name] = dict(achieved=gbs, ms=ms, launches=n, bytes=byt)
+    h_ms, h_n, h_items = prof["experts_hit"]
+    m_ms, m_n, m_items = prof["experts_miss"]
+    r_ms, r_n, _ = prof["router"]
+    out["experts_hit"] = dict(ms=h_ms, launches=h_n, bytes=h_items * eb,
+                              achieved=(h_items * eb / (h_ms / 1e3) / 1e9) if h_ms > 0 else 0.0)
+    out["experts_miss"] = dict(ms=m_ms, launches=m_n, hbm_bytes=m_items * eb)
+    route_per_call = r_ms / r_n if r_n else 0.0
+    t_m2 = h_ms + route_per_call * h_n
+    b_m2 = h_items * eb + h_n * router_bytes
+    out["step_m2"] = dict(bytes=b_m2, ms=t_m2,
+                          achieved=(b_m2 / (t_m2 / 1e3) / 1e9) if t_m2 > 0 else 0.0)
+    out["route_us_per_call"] = route_per_call * 1e3
     return out
 
 
@@ -393,8 +424,10 @@ def run_decode(args, wl, rank, world):
     pk = peaks()
     seed = SEED + rank
     pool = build_pool(wl, seed)
+    h2d_gbs = measure_h2d()
     per_batch = {}
     head = None
+    eb = entry_bytes(wl)
     for b in wl["batches"]:
         res, x_all, bias_all = bench_decode_batch(wl, pool, b, args.warmup, args.steps, seed,
                                                   world)
@@ -403,45 +436,60 @@ def run_decode(args, wl, rank, world):
         prof_k = min(args.steps, args.profile_steps)
         prof, touched, fill_bytes, n_calls = profile_decode_batch(
             wl, pool, b, x_all, bias_all, args.warmup, prof_k, seed)
-        rl = roofline_decode(wl, prof, touched, n_calls, pk)
-        fill_ms = prof["fill"][0]
-        res["kernels_ms_per_step"] = {c: v[0] / prof_k for c, v in prof.items()}
-        res["gateup_gbs"] = rl["gateup"]["achieved"]
-        res["down_gbs"] = rl["down"]["achieved"]
-        res["fill_gbs"] = fill_bytes / (fill_ms / 1e3) / 1e9 if fill_ms > 0 else None
+        rl = roofline_decode(wl, prof, pk)
+        res["kernels_ms_per_step"] = {c: v[0] / prof_k for c, v in prof.items() if v[1]}
+        res["launches_per_step"] = {c: v[1] / prof_k for c, v in prof.items() if v[1]}
+        res["experts_hit_gbs"] = rl["experts_hit"]["achieved"]
+        res["step_m2_gbs"] = rl["step_m2"]["achieved"]
+        res["route_us_per_call"] = rl["route_us_per_call"]
+        miss_ms = rl["experts_miss"]["ms"]
+        res["fill_gbs"] = fill_bytes / (miss_ms / 1e3) / 1e9 if miss_ms > 0 else None
         e2e = bench_decode_e2e(wl, pool, b, x_all, bias_all, args.warmup, args.steps, seed, world)
         e2e["ms"] = max_over_ranks(e2e["ms"], world)
         res["e2e_tok_s_all"] = world * b * args.steps / (e2e["ms"] / 1e3)
         res["e2e"] = e2e
         per_batch[b] = res
         if b == wl["headline_b"]:
-            head = (res, rl, prof, prof_k, bias_all)
+            head = (res, rl, prof, prof_k, bias_all, fill_bytes)
         del x_all, bias_all
         torch.cuda.empty_cache()
-    res, rl, prof, prof_k, bias_all = head
+    res, rl, prof, prof_k, bias_all, fill_bytes = head
     b = wl["headline_b"]
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         calls, el = cpu_oracle_decode(wl, pool, b, bias_all.cpu().numpy(), seed,
                                       budget_s=args.cpu_budget)
         cpu = {"value": b * calls / wl["L"] / el, "unit": "tokens/s", "cores": 1,
-               "kind": "oracle",
+               "kind": "oracle", "host_cores": os.cpu_count(),
                "sample": f"first {calls} layer calls of the b={b} trace "
                          f"({calls / wl['L']:.2f} decode steps), {el:.1f} s, numpy fp32 router "
-                         f"+ fp64 experts, single thread"}
-    g = rl["gateup"]
-    # DRAM bytes per launch of k_gateup_tma at b = 1 (8 touched experts) from the committed ncu
-    # capture of the decode kernels; only valid for that shape and the bf16 kernel
-    traffic = (50.56e6 if (args.workload == "decode24" and b == 1 and not wl.get("fp4"))
-               else None)  # ncu, per launch
-    kname = "k_gateup_fp4" if wl.get("fp4") else "k_gateup_tma"
-    roof = {"bound": "hbm", "kernel": f"{kname} (gate/up + SwiGLU, decode)",
-            "achieved": round(g["achieved"], 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
-            "frac": round(g["achieved"] / pk["hbm_gbs"], 4), "traffic": traffic,
+                         f"+ fp64 experts, single thread (the box has {os.cpu_count()} cores)"}
+    eh = rl["experts_hit"]
+    kname = "k_decode_experts<mxfp4>" if wl.get("fp4") else "k_decode_experts"
+    traffic = None
+    if args.workload == "decode24" and b == 1 and not wl.get("fp4") and TRAFFIC_DECODE24_B1:
+        traffic = TRAFFIC_DECODE24_B1
+    roof = {"bound": "hbm",
+            "kernel": f"{kname} (gate/up + SwiGLU + down + combine; fills when the call misses), "
+                      "launches of calls without misses",
+            "achieved": round(eh["achieved"], 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+            "frac": round(eh["achieved"] / pk["hbm_gbs"], 4), "traffic": traffic,
             "peak_source": pk["source"],
-            "algorithmic_bytes": ("touched experts x 2*d_ff*d*17/32 B per call (MXFP4 codes "
-                                  "+ scales)" if wl.get("fp4") else
-                                  "touched experts x 2*d_ff*d*2 B per call (50.33 MB at b=1)")}
+            "frac_of_8tbs": round(eh["achieved"] / 8000.0, 4),
+            "launches": eh["launches"],
+            "algorithmic_bytes": ("entries streamed x 3*d*d_ff*17/32 B (MXFP4 codes + scales)"
+                                  if wl.get("fp4") else
+                                  f"entries streamed x 3*d*d_ff*2 B = {eb / 1e6:.2f} MB per entry"
+                                  " (touched experts + shared)")}
+    m2 = rl["step_m2"]
+    fill = {"fill_gbs": round(fill_bytes / (rl["experts_miss"]["ms"] / 1e3) / 1e9, 2)
+            if rl["experts_miss"]["ms"] > 0 else None,
+            "h2d_gbs": round(h2d_gbs, 2),
+            "h2d_how": "pinned cudaMemcpyAsync host -> device of 1 GiB, best of 5, this run",
+            "fill_how": "missed-entry bytes over the time of the expert launches of calls with "
+                        "misses (their hit experts overlap the fills)"}
+    if fill["fill_gbs"]:
+        fill["frac"] = round(fill["fill_gbs"] / h2d_gbs, 4)
     line = {
         "metric": "MoE-layer tokens/s (decode trace, b=1"
                   + (", MXFP4 experts" if wl.get("fp4") else "")
@@ -458,30 +506,49 @@ def run_decode(args, wl, rank, world):
                    "admission": bool(wl.get("admission")),
                    "weights": "mxfp4" if wl.get("fp4") else "bf16",
                    "l2": "inputs larger than L2 (every step streams "
-                         f">{wl['L'] * wl['k'] * entry_bytes(wl) / 1e9:.2f} GB of experts)",
+                         f">{wl['L'] * wl['k'] * eb / 1e9:.2f} GB of experts)",
                    "parallelism": f"replicas x{world}",
                    "per_batch": {str(bb): {k: (round(v, 4) if isinstance(v, float) else v)
                                            for k, v in r.items()
                                            if k not in ("clocks", "e2e")}
                                  for bb, r in per_batch.items()}},
         "roofline": roof,
-        "roofline_down": {"achieved": round(rl["down"]["achieved"], 1), "unit": "GB/s",
-                          "frac": round(rl["down"]["achieved"] / pk["hbm_gbs"], 4)},
+        "decode_step_m2": {"achieved": round(m2["achieved"], 1), "unit": "GB/s",
+                           "frac": round(m2["achieved"] / pk["hbm_gbs"], 4),
+                           "frac_of_8tbs": round(m2["achieved"] / 8000.0, 4),
+                           "what": "touched entries + router weights over routing + expert "
+                                   "kernel time, calls without misses"},
+        "fill": fill,
         "cpu_baseline": cpu,
         "e2e": {"value": round(res["e2e_tok_s_all"], 2), "unit": "tokens/s",
                 "h2d_bytes_per_step": res["e2e"]["h2d"], "d2h_bytes_per_step": res["e2e"]["d2h"]},
-        # kernels per decode layer call: routing, fill, gate/up, down, combine (one timing
-        # scope each)
+        # kernels per decode layer call: routing + control, and the expert kernel
         "gpu_launches": int(sum(v[1] for v in prof.values()) / prof_k * args.steps),
         "clocks": res["clocks"],
     }
+    if args.workload == "decode24" and not args.no_prefill and not wl.get("fp4"):
+        del pool
+        import gc
+        gc.collect()
+        if hasattr(torch._C, "_host_emptyCache"):
+            torch._C._host_emptyCache()
+        pl = run_prefill(args, dict(WORKLOADS["prefill8"]), rank, world, steps=1)
+        line["prefill"] = {t: {k: v for k, v in r.items()
+                               if k in ("tok_s", "ms_per_prefill", "gemm_ms_per_layer",
+                                        "gemm_tflops", "tc_frac", "tc_frac_sustained",
+                                        "overlap", "h2d_gbs", "copy_ms", "compute_ms",
+                                        "wall_ms", "router_ms_per_layer")}
+                           for t, r in pl["config"]["per_T"].items()}
+        line["prefill"]["workload"] = "prefill8: 8 layers, d=4096, d_ff=2048, E=256, top-6"
+        line["prefill"]["peak_tflops"] = pk["bf16"]
+        line["prefill"]["peak_tflops_sustained"] = pk["bf16_sustained"]
     return line
 
 
 # ----------------------------------------------------------------------------------------
 # prefill benchmark
 # ----------------------------------------------------------------------------------------
-def run_prefill(args, wl, rank, world):
+def run_prefill(args, wl, rank, world, steps=None):
     """Prefill streaming: every layer's full expert set is copied host -> device into the back
     buffer while the previous layer computes.  A step is one prefill over all L layers."""
     import torch
@@ -490,7 +557,7 @@ def run_prefill(args, wl, rank, world):
     seed = SEED + rank
     pool = build_pool(wl, seed)
     L, d, d_ff, k = wl["L"], wl["d"], wl["d_ff"], wl["k"]
-    K = max(1, min(args.steps, args.prefill_steps))
+    K = steps or max(1, min(args.steps, args.prefill_steps))
     W = 1
     per_T = {}
     for T in wl["tokens"]:
@@ -525,11 +592,15 @@ def run_prefill(args, wl, rank, world):
         flops = 2.0 * 3 * d * d_ff * T * k * L
         gemm_ms = prof["gateup"][0] + prof["down"][0]
         tflops = flops / (gemm_ms / 1e3) / 1e12 if gemm_ms > 0 else 0.0
+        router_ms = prof["router"][0] + prof["topk"][0] + prof["control"][0]
         overlap = (copy_ms + comp_ms - wall_ms) / max(1e-9, min(copy_ms, comp_ms))
         h2d_b, d2d_b = st.prefill_bytes()
         per_T[T] = dict(ms_per_prefill=ms / K, tok_s=world * T * K / (ms / 1e3),
                         gemm_ms_per_layer=gemm_ms / L, gemm_tflops=tflops,
-                        tc_frac=tflops / pk["bf16"], copy_ms=copy_ms / K,
+                        tc_frac=tflops / pk["bf16"],
+                        tc_frac_sustained=tflops / pk["bf16_sustained"]
+                        if pk.get("bf16_sustained") else None,
+                        router_ms_per_layer=router_ms / L, copy_ms=copy_ms / K,
                         compute_ms=comp_ms / K, wall_ms=wall_ms / K, overlap=overlap,
                         h2d_gbs=h2d_b / (copy_ms / K / 1e3) / 1e9,
                         h2d_gb_per_prefill=h2d_b / 1e9, d2d_gb_per_prefill=d2d_b / 1e9,
@@ -753,6 +824,8 @@ def main():
     ap.add_argument("--prefill-steps", type=int, default=2)
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true",
+                    help="leave the prefill block out of the decode line")
     ap.add_argument("--batches", default="", help="comma list of decode batch sizes")
     ap.add_argument("--slots", type=int, default=0, help="override the slot count")
     ap.add_argument("--fp4", action="store_true",

@@ -28,12 +28,15 @@ EXPORTS = [
     "ft_moe_prefill_timing", "ft_cache_resize",
     "ft_cache_stats", "ft_cache_stats_reset", "ft_moe_status", "ft_moe_get_routing",
     "ft_moe_get_logits", "ft_moe_get_perm", "ft_moe_get_cache_state", "ft_moe_get_fills",
-    "ft_moe_get_dims", "ft_moe_profile", "ft_moe_profile_read", "ft_route_topk_noalloc",
+    "ft_moe_get_dims", "ft_moe_profile", "ft_moe_profile_read", "ft_moe_debug_set",
+    "ft_route_topk_noalloc",
 ]
 
 FT_WEIGHTS_BF16, FT_WEIGHTS_MXFP4 = 0, 1
 
-PROF_CLASSES = ["router", "topk", "control", "fill", "gateup", "down", "other"]
+PROF_CLASSES = ["router", "topk", "control", "fill", "gateup", "down", "other",
+                "experts_hit", "experts_miss"]
+FT_DEBUG_HOLD_FILLS, FT_DEBUG_WAIT_NS = 1, 2
 
 
 class FtError(RuntimeError):
@@ -103,7 +106,8 @@ def load_library(path: str = LIB_PATH):
         "ft_moe_get_fills": (I, [P, ctypes.POINTER(ctypes.c_int32), P, I]),
         "ft_moe_get_dims": (I, [P, P]),
         "ft_moe_profile": (I, [P, I]),
-        "ft_moe_profile_read": (I, [P, P, P]),
+        "ft_moe_profile_read": (I, [P, P, P, P]),
+        "ft_moe_debug_set": (I, [P, I, ctypes.c_int64]),
         "ft_route_topk_noalloc": (I, [P, P, P, I, I, I, I, P, P, P, P]),
     }
     for name, (res, args) in sig.items():
@@ -280,12 +284,19 @@ def ft_moe_profile(h, enable):
 
 
 def ft_moe_profile_read(h) -> dict:
-    """{class: (total ms, launches)} since the last read."""
+    """{class: (total ms, launches, expert entries processed)} since the last read."""
     import numpy as np
     ms = np.zeros(len(PROF_CLASSES), np.float64)
     n = np.zeros(len(PROF_CLASSES), np.int64)
-    _check(load_library().ft_moe_profile_read(h, ms.ctypes.data, n.ctypes.data))
-    return {c: (float(ms[i]), int(n[i])) for i, c in enumerate(PROF_CLASSES)}
+    items = np.zeros(len(PROF_CLASSES), np.int64)
+    _check(load_library().ft_moe_profile_read(h, ms.ctypes.data, n.ctypes.data,
+                                              items.ctypes.data))
+    return {c: (float(ms[i]), int(n[i]), int(items[i])) for i, c in enumerate(PROF_CLASSES)}
+
+
+def ft_moe_debug_set(h, what, value):
+    """Test hooks: FT_DEBUG_HOLD_FILLS (fills never reported done), FT_DEBUG_WAIT_NS."""
+    _check(load_library().ft_moe_debug_set(h, what, int(value)))
 
 
 def ft_route_topk_noalloc(x, wr, bias, T, E, d, k, idx, w, tie, stream=None):
@@ -379,3 +390,6 @@ class MoELayerStack:
 
     def profile_read(self):
         return ft_moe_profile_read(self.h)
+
+    def debug_set(self, what, value):
+        ft_moe_debug_set(self.h, what, value)

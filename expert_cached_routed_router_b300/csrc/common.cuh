@@ -31,6 +31,10 @@ constexpr int kMaxE = 1024;        // experts per layer
 constexpr int kMaxK = 32;          // routed experts per token
 constexpr int kGemvMaxTokens = 16; // forward calls with T <= this use the GEMV kernels
 constexpr double kNearTie = 1e-6;  // top-k gap reported as a near-tie (exact fp32 difference)
+// Default limit of a cross-CTA wait in the decode expert kernel.  The longest legitimate wait
+// is for the last fill of a call, behind every other fill of that call over the host link
+// (about 0.1 s for 96 misses of 50 MB); a wait that runs out records FT_ERR_TIMEOUT.
+constexpr unsigned long long kDefaultWaitNs = 4000000000ull;
 
 // Device counters and the status word.  One instance per handle, in device memory.
 struct DevCounters {
@@ -44,7 +48,13 @@ struct DevCounters {
   int occupied;                  // slots holding an entry
   int call_status;               // 0, or FT_ERR_CAPACITY if the current call was refused
   unsigned route_arrive;         // CTAs of the fused routing kernel that have finished
-  int pad[2];
+  int n_hit;                     // work items 0 .. n_hit-1 are cached hits; the n_fill
+                                 // misses follow (item n_hit + m uses fill m), then the
+                                 // shared expert
+  int hold_fills;                // debug: the decode expert kernel never reports its fills
+                                 // done, so its waits for them run out (timeout tests)
+  int pad;
+  unsigned long long wait_ns;    // limit of every cross-CTA wait of the decode expert kernel
 };
 
 // Where the cache's slot state lives.  Kept in device memory and read by the kernels on
@@ -88,6 +98,8 @@ struct ControlArgs {
   const CacheDesc *cache;      // slot storage, owners, stamps, capacity (device)
   int32_t *fills;       // [max_fill][3]
   uint32_t *freq;       // admission counts [L][E], or null for the plain LRU
+  int32_t *sync;        // decode expert kernel counters, zeroed here ([n_sync])
+  int n_sync;
   const uint16_t *buffer;      // prefill: E entries of this layer
   const uint16_t *shared;      // shared entry of this layer or null
   size_t entry_elems;
@@ -103,6 +115,20 @@ __device__ __forceinline__ uint16_t f32_to_bf16(float f) {
   uint32_t u = __float_as_uint(f);
   u += 0x7FFFu + ((u >> 16) & 1u);
   return (uint16_t)(u >> 16);
+}
+
+// E2M1 code (low 4 bits of c) -> fp32: the sign goes to bit 31 and the three magnitude bits
+// (2 exponent, 1 mantissa) to bits 22..24, which is the value times 2^-126 (a subnormal when
+// the exponent field is 0); one exact multiply by 2^126 restores it.  Relies on fp32
+// subnormals being kept (no flush-to-zero build flags).
+__device__ __forceinline__ float e2m1_f32(uint32_t c) {
+  return __uint_as_float(((c & 8u) << 28) | ((c & 7u) << 22)) * 0x1p126f;
+}
+
+// E8M0 scale byte -> 2^(s - 127); s = 255 is NaN.
+__device__ __forceinline__ float e8m0_f32(uint32_t s) {
+  return s == 0 ? __uint_as_float(0x00400000u)
+                : (s == 255 ? __uint_as_float(0x7FC00000u) : __uint_as_float(s << 23));
 }
 
 // Programmatic dependent launch: let the next kernel on the stream start launching now, and

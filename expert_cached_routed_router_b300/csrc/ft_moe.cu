@@ -81,10 +81,13 @@ struct ft_moe {
   uint16_t *xp = nullptr;
   float *acc = nullptr;
   float *ybuf = nullptr;  // decode: fp32 rows of the down projection [(16k + 16)][d]
+  int32_t *sync = nullptr;  // decode expert kernel completion counters [kSyncInts(d)]
   int32_t *chunk = nullptr;
   int *tile_prefix = nullptr;  // tcgen05 tile scheduler [kMaxE + 3]
   TcMaps maps_slots{};         // tensor maps over the slot storage
   TcMaps maps_dbuf[2]{};       // ... over the prefill double buffer
+  uint16_t *fp4_scratch = nullptr;  // MXFP4 entries expanded to bf16 for the grouped GEMMs [E]
+  TcMaps maps_fp4{};                // ... and its tensor maps
   uint64_t resizes = 0;
 
   // pool
@@ -95,6 +98,7 @@ struct ft_moe {
 
   // prefill
   uint16_t *dbuf[2] = {nullptr, nullptr};
+  uint16_t *chain[2] = {nullptr, nullptr};  // residual stream inputs of layers 1.. [max_tokens][d]
   cudaStream_t copy_stream = nullptr;
   std::vector<cudaEvent_t> ev_cs, ev_ce, ev_ks, ev_ke;  // copy start/end, compute start/end
   int last_prefill_layers = 0;
@@ -119,6 +123,10 @@ struct ft_moe {
   bool prof_keep = false;                     // graph mode: keep the recorded pairs
   std::vector<cudaEvent_t> prof_events;       // pool; pairs (begin, end)
   std::vector<int> prof_class;                // class of pair i
+  int32_t *prof_rec = nullptr;                // device [pairs][2]: (n_fill, n_work) of the
+                                              // call of a decode expert launch
+  size_t prof_rec_cap = 0;
+  int64_t prof_items[FT_PROF_N] = {};
   double prof_ms[FT_PROF_N] = {};
   int64_t prof_n[FT_PROF_N] = {};
 };
@@ -147,11 +155,24 @@ int alloc_n(ft_moe *h, T **p, size_t n) {
 void prof_flush(ft_moe *h) {
   if (h->prof_class.empty()) return;
   cudaEventSynchronize(h->prof_events[2 * h->prof_class.size() - 1]);
+  std::vector<int32_t> rec;
+  if (h->prof_rec) {
+    rec.resize(2 * std::min(h->prof_class.size(), h->prof_rec_cap));
+    if (cudaMemcpy(rec.data(), h->prof_rec, rec.size() * 4, cudaMemcpyDeviceToHost) != cudaSuccess)
+      rec.clear();
+  }
   for (size_t i = 0; i < h->prof_class.size(); ++i) {
     float ms = 0.f;
+    int cls = h->prof_class[i];
+    int64_t items = 0;
+    if (cls == FT_PROF_EXPERTS_HIT && 2 * i + 1 < rec.size()) {
+      if (rec[2 * i] > 0) cls = FT_PROF_EXPERTS_MISS;
+      items = rec[2 * i + 1];
+    }
     if (cudaEventElapsedTime(&ms, h->prof_events[2 * i], h->prof_events[2 * i + 1]) == cudaSuccess) {
-      h->prof_ms[h->prof_class[i]] += ms;
-      h->prof_n[h->prof_class[i]] += 1;
+      h->prof_ms[cls] += ms;
+      h->prof_n[cls] += 1;
+      h->prof_items[cls] += items;
     }
   }
   cudaGetLastError();
@@ -181,7 +202,12 @@ struct ProfScope {
     record(h->prof_events[2 * idx]);
   }
   ~ProfScope() {
-    if (idx >= 0) record(h->prof_events[2 * idx + 1]);
+    if (idx < 0) return;
+    record(h->prof_events[2 * idx + 1]);
+    // the decode expert kernel's call: its fill and item counts, read back at the flush
+    if (h->prof_class[idx] == FT_PROF_EXPERTS_HIT && h->prof_rec && (size_t)idx < h->prof_rec_cap)
+      cudaMemcpyAsync(h->prof_rec + 2 * idx, &h->ctr->n_fill, 2 * sizeof(int32_t),
+                      cudaMemcpyDeviceToDevice, s);
   }
   // In graph mode the records are captured as external event nodes, which keep timing.
   void record(cudaEvent_t e) {
@@ -198,8 +224,11 @@ void free_all(ft_moe *h) {
   if (h->slots) cudaFree(h->slots);
   if (h->owner) cudaFree(h->owner);
   if (h->stamps) cudaFree(h->stamps);
-  for (int i = 0; i < 2; ++i)
+  if (h->fp4_scratch) cudaFree(h->fp4_scratch);
+  for (int i = 0; i < 2; ++i) {
     if (h->dbuf[i]) cudaFree(h->dbuf[i]);
+    if (h->chain[i]) cudaFree(h->chain[i]);
+  }
   if (h->xstage) cudaFree(h->xstage);
   if (h->ostage) cudaFree(h->ostage);
   for (auto *v : {&h->ev_cs, &h->ev_ce, &h->ev_ks, &h->ev_ke})
@@ -207,6 +236,7 @@ void free_all(ft_moe *h) {
   if (h->copy_stream) cudaStreamDestroy(h->copy_stream);
   if (h->pool_registered) cudaHostUnregister(const_cast<uint16_t *>(h->pool_host));
   for (cudaEvent_t e : h->prof_events) cudaEventDestroy(e);
+  if (h->prof_rec) cudaFree(h->prof_rec);
 }
 
 bool capturing(cudaStream_t s) {
@@ -240,6 +270,8 @@ ControlArgs control_args(ft_moe *h, int layer, int T, bool decode, const uint16_
   a.cache = h->cache;
   a.fills = h->fills;
   a.freq = h->freq;
+  a.sync = decode ? h->sync : nullptr;
+  a.n_sync = decode ? kSyncInts(h->d) : 0;
   a.buffer = buffer;
   a.shared = h->n_shared ? h->shared + (size_t)layer * h->entry_elems : nullptr;
   a.entry_elems = h->entry_elems;
@@ -272,6 +304,19 @@ int build_maps(ft_moe *h, TcMaps *m, const uint16_t *buffer, int n_entries) {
          make_tmap(&m->bs_dn256, sh, f, nsh * 3 * d, 256);
   if (!ok) return fail(FT_ERR_CUDA, "cuTensorMapEncodeTiled failed");
   return FT_OK;
+}
+
+// bf16 scratch for the MXFP4 entries of one grouped-GEMM call (E entries) and its maps.
+int ensure_fp4_scratch(ft_moe *h) {
+  if (h->fp4_scratch) return FT_OK;
+  const size_t bytes = (size_t)h->E * 6 * h->d * h->d_ff;
+  cudaError_t e = cudaMalloc(&h->fp4_scratch, bytes);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    h->fp4_scratch = nullptr;
+    return fail(FT_ERR_OOM, "MXFP4 expansion scratch (%zu bytes): %s", bytes, cudaGetErrorString(e));
+  }
+  return build_maps(h, &h->maps_fp4, h->fp4_scratch, h->E);
 }
 
 // Router, top-k, permutation and control for one layer.
@@ -307,37 +352,60 @@ void route_layer(ft_moe *h, int layer, const uint16_t *x, int T, bool decode,
 }
 
 // Expert FFN + combine for one layer after routing; `maps` view the weights' buffer.
-void experts_layer(ft_moe *h, const uint16_t *x, int T, uint16_t *out, const TcMaps &maps,
-                   int layer, cudaStream_t s) {
+// Decode calls (T <= kGemvMaxTokens) run the fills and the whole expert path in one launch;
+// larger calls fill first (decode forward) and then run the grouped GEMMs, as does every
+// prefill layer (whose cast also writes the residual stream's next input).
+int experts_layer(ft_moe *h, const uint16_t *x, int T, uint16_t *out, const TcMaps &maps,
+                  int layer, bool decode, cudaStream_t s, uint16_t *next = nullptr) {
   const int P = T * h->k;
-  const int max_work = std::min(h->E, P) + h->n_shared;
-  if (T <= kGemvMaxTokens) {
-    {
-      ProfScope p(h, FT_PROF_GATEUP, s);
-      launch_gateup_gemv(h->work, h->ctr, max_work, x, h->tok, h->hbuf, T, h->d, h->d_ff, h->fp4,
-                         s);
-    }
-    {
-      ProfScope p(h, FT_PROF_DOWN, s);
-      launch_down_gemv(h->work, h->ctr, max_work, h->hbuf, h->ybuf, T, h->d, h->d_ff, h->fp4, s);
-    }
-    ProfScope p(h, FT_PROF_OTHER, s);
-    launch_combine(h->ybuf, h->w, h->inv, h->ctr, out, T, h->k, h->d, h->n_shared, s);
-  } else {
-    const int rows = P + (h->n_shared ? T : 0);
-    {
-      ProfScope p(h, FT_PROF_OTHER, s);
-      launch_gather_rows(x, h->tok, h->xp, rows, h->d, h->ctr, s);
-      cudaMemsetAsync(h->acc, 0, (size_t)T * h->d * sizeof(float), s);
-    }
-    {
-      ProfScope p(h, FT_PROF_GATEUP, s);  // gate/up and down GEMMs on the tensor cores
-      launch_tc_ffn(maps, h->work, h->ctr, h->tile_prefix, h->hbuf, h->tok, h->wq, h->acc, h->d,
-                    h->d_ff, layer, s);
-    }
-    ProfScope p(h, FT_PROF_OTHER, s);
-    launch_cast_out(h->acc, out, (size_t)T * h->d, h->ctr, s);
+  if (decode && T <= kGemvMaxTokens) {
+    DecodeArgs a{};
+    a.work = h->work;
+    a.ctr = h->ctr;
+    a.fills = h->fills;
+    a.pool = reinterpret_cast<const uint4 *>(h->pool_dev);
+    a.cache = h->cache;
+    a.x = x;
+    a.tok = h->tok;
+    a.w = h->w;
+    a.inv = h->inv;
+    a.h = h->hbuf;
+    a.y = h->ybuf;
+    a.out = out;
+    a.sync = h->sync;
+    a.T = T;
+    a.k = h->k;
+    a.d = h->d;
+    a.d_ff = h->d_ff;
+    a.E = h->E;
+    a.shared = h->n_shared;
+    a.entry_bytes = h->entry_bytes;
+    ProfScope p(h, FT_PROF_EXPERTS_HIT, s);
+    return launch_decode_experts(a, h->fp4, s);
   }
+  if (decode) {
+    ProfScope p(h, FT_PROF_FILL, s);
+    launch_fill(h->pool_dev, h->cache, h->fills, h->ctr, h->entry_bytes, h->E,
+                std::min(h->E, P), s);
+  }
+  const int rows = P + (h->n_shared ? T : 0);
+  {
+    ProfScope p(h, FT_PROF_OTHER, s);
+    launch_gather_rows(x, h->tok, h->xp, rows, h->d, h->ctr, s);
+    cudaMemsetAsync(h->acc, 0, (size_t)T * h->d * sizeof(float), s);
+  }
+  if (h->fp4) {
+    ProfScope p(h, FT_PROF_OTHER, s);
+    launch_dequant_work(h->work, h->ctr, h->fp4_scratch, h->d, h->d_ff, std::min(h->E, P), s);
+  }
+  {
+    ProfScope p(h, FT_PROF_GATEUP, s);  // gate/up and down GEMMs on the tensor cores
+    launch_tc_ffn(h->fp4 ? h->maps_fp4 : maps, h->work, h->ctr, h->tile_prefix, h->hbuf, h->tok,
+                  h->wq, h->acc, h->d, h->d_ff, layer, h->fp4, s);
+  }
+  ProfScope p(h, FT_PROF_OTHER, s);
+  launch_cast_out(h->acc, out, (size_t)T * h->d, x, next, h->ctr, s);
+  return FT_OK;
 }
 
 int check_handle(ft_moe *h) {
@@ -421,6 +489,7 @@ int ft_moe_create(int L, int E, int k, int d, int d_ff, int n_slots, const ft_mo
   A(alloc_n(h, &h->xp, R * d));
   A(alloc_n(h, &h->acc, T * d));
   A(alloc_n(h, &h->ybuf, (size_t)(kGemvMaxTokens * k + kGemvMaxTokens) * d));
+  A(alloc_n(h, &h->sync, (size_t)kSyncInts(d)));
   A(alloc_n(h, &h->chunk, perm_multi_scratch_ints((int)P, E)));
   A(alloc_n(h, &h->tile_prefix, (size_t)kMaxE + 3));
   if (h->admission) A(alloc_n(h, &h->freq, (size_t)L * E));
@@ -441,6 +510,11 @@ int ft_moe_create(int L, int E, int k, int d, int d_ff, int n_slots, const ft_mo
     if (e == cudaSuccess) e = cudaMemset(h->owner, 0xFF, (size_t)n_slots * sizeof(int32_t));
     if (e == cudaSuccess) e = cudaMemset(h->stamps, 0, (size_t)n_slots * sizeof(unsigned long long));
     if (e == cudaSuccess) e = cudaMemset(h->ctr, 0, sizeof(DevCounters));
+    if (e == cudaSuccess) e = cudaMemset(h->sync, 0, (size_t)kSyncInts(d) * sizeof(int32_t));
+    if (e == cudaSuccess) {
+      const unsigned long long limit = kDefaultWaitNs;
+      e = cudaMemcpy(&h->ctr->wait_ns, &limit, sizeof(limit), cudaMemcpyHostToDevice);
+    }
     if (e == cudaSuccess && h->freq) e = cudaMemset(h->freq, 0, (size_t)L * E * sizeof(uint32_t));
     if (e == cudaSuccess) e = cudaMemset(h->wr, 0, (size_t)L * E * d * 2);
     if (e == cudaSuccess && h->shared) e = cudaMemset(h->shared, 0, (size_t)L * h->entry_bytes);
@@ -449,6 +523,9 @@ int ft_moe_create(int L, int E, int k, int d, int d_ff, int n_slots, const ft_mo
     if (e != cudaSuccess) rc = fail(FT_ERR_CUDA, "initialisation: %s", cudaGetErrorString(e));
   }
   if (rc == FT_OK && !h->fp4) rc = build_maps(h, &h->maps_slots, h->slots, n_slots + h->n_stage);
+  // MXFP4 calls with more tokens than the decode path takes expand their entries to bf16
+  // first; the scratch exists from creation so that such calls can be captured
+  if (rc == FT_OK && h->fp4 && h->max_tokens > kGemvMaxTokens) rc = ensure_fp4_scratch(h);
   if (rc == FT_OK) rc = upload_cache_desc(h);
   if (rc != FT_OK) {
     free_all(h);
@@ -577,18 +654,11 @@ int ft_moe_forward(ft_moe *h, int layer, const void *x, int T, void *out, ft_str
   if (!x || !out) return fail(FT_ERR_INVALID, "x or out is NULL");
   if ((((uintptr_t)x) | ((uintptr_t)out)) & 15)
     return fail(FT_ERR_INVALID, "x and out must be 16-byte aligned");
-  if (h->fp4 && T > kGemvMaxTokens)
-    return fail(FT_ERR_INVALID, "MXFP4 entries: decode calls only (T <= %d, got %d)",
-                kGemvMaxTokens, T);
   cudaStream_t s = (cudaStream_t)stream;
   const uint16_t *xb = static_cast<const uint16_t *>(x);
   route_layer(h, layer, xb, T, true, nullptr, s);
-  {
-    ProfScope p(h, FT_PROF_FILL, s);
-    launch_fill(h->pool_dev, h->cache, h->fills, h->ctr, h->entry_bytes, h->E,
-                std::min(h->E, T * h->k), s);
-  }
-  experts_layer(h, xb, T, static_cast<uint16_t *>(out), h->maps_slots, layer, s);
+  if (int r = experts_layer(h, xb, T, static_cast<uint16_t *>(out), h->maps_slots, layer, true, s))
+    return r;
   h->last_T = T;
   h->last_stream = s;
   cudaError_t e = cudaGetLastError();
@@ -636,7 +706,6 @@ int ft_moe_prefill_stream(ft_moe *h, int layer0, int n_layers, const void *x, in
                           ft_stream_t stream) {
   if (int r = check_handle(h)) return r;
   if (!h->pool_host) return fail(FT_ERR_STATE, "prefill before ft_moe_load_pool");
-  if (h->fp4) return fail(FT_ERR_INVALID, "MXFP4 entries: prefill is not supported");
   if (n_layers < 1 || layer0 < 0 || layer0 + n_layers > h->L)
     return fail(FT_ERR_INVALID, "layers [%d, %d) out of range", layer0, layer0 + n_layers);
   if (T < 1 || T > h->max_tokens)
@@ -657,9 +726,20 @@ int ft_moe_prefill_stream(ft_moe *h, int layer0, int n_layers, const void *x, in
         return fail(FT_ERR_OOM, "double buffer (%zu bytes): %s", layer_bytes,
                     cudaGetErrorString(e));
       }
-      if (int r = build_maps(h, &h->maps_dbuf[i], h->dbuf[i], h->E)) return r;
+      if (!h->fp4)
+        if (int r = build_maps(h, &h->maps_dbuf[i], h->dbuf[i], h->E)) return r;
+    }
+    if (!h->chain[i]) {
+      cudaError_t e = cudaMalloc(&h->chain[i], (size_t)h->max_tokens * h->d * 2);
+      if (e != cudaSuccess) {
+        cudaGetLastError();
+        h->chain[i] = nullptr;
+        return fail(FT_ERR_OOM, "residual stream buffer: %s", cudaGetErrorString(e));
+      }
     }
   }
+  if (h->fp4)
+    if (int r = ensure_fp4_scratch(h)) return r;
   while ((int)h->ev_cs.size() < n_layers) {
     cudaEvent_t a, b, c, d;
     FT_CUDA(cudaEventCreate(&a));
@@ -727,8 +807,14 @@ int ft_moe_prefill_stream(ft_moe *h, int layer0, int n_layers, const void *x, in
       if (int r = enqueue_copy(i + 1)) return r;
     FT_CUDA(cudaStreamWaitEvent(s, h->ev_ce[i], 0));
     FT_CUDA(cudaEventRecord(h->ev_ks[i], s));
-    route_layer(h, layer0 + i, xb, T, false, h->dbuf[i & 1], s);
-    experts_layer(h, xb, T, ob + (size_t)i * T * h->d, h->maps_dbuf[i & 1], layer0 + i, s);
+    // residual stream: layer i reads x_i (x_0 = x), and writes out[i] = y_i and
+    // x_{i+1} = bf16(x_i + y_i) for the next layer
+    const uint16_t *xi = i == 0 ? xb : h->chain[i & 1];
+    uint16_t *xnext = i + 1 < n_layers ? h->chain[(i + 1) & 1] : nullptr;
+    route_layer(h, layer0 + i, xi, T, false, h->dbuf[i & 1], s);
+    if (int r = experts_layer(h, xi, T, ob + (size_t)i * T * h->d, h->maps_dbuf[i & 1], layer0 + i,
+                              false, s, xnext))
+      return r;
     FT_CUDA(cudaEventRecord(h->ev_ke[i], s));
   }
   h->last_prefill_layers = n_layers;
@@ -958,20 +1044,43 @@ int ft_moe_profile(ft_moe *h, int enable) {
         h->prof_events.push_back(e);
       }
     }
+    if (!h->prof_rec) {  // one record per event pair, for every pair the pool can hold
+      h->prof_rec_cap = 8192;
+      FT_CUDA(cudaMalloc(&h->prof_rec, h->prof_rec_cap * 2 * sizeof(int32_t)));
+      FT_CUDA(cudaMemset(h->prof_rec, 0, h->prof_rec_cap * 2 * sizeof(int32_t)));
+    }
     h->prof_keep = enable == 2;
   }
   h->prof_on = enable != 0;
   return FT_OK;
 }
 
-int ft_moe_profile_read(ft_moe *h, double *ms, int64_t *launches) {
+int ft_moe_profile_read(ft_moe *h, double *ms, int64_t *launches, int64_t *items) {
   if (int r = check_handle(h)) return r;
   prof_flush(h);
   for (int i = 0; i < FT_PROF_N; ++i) {
     if (ms) ms[i] += h->prof_ms[i];
     if (launches) launches[i] += h->prof_n[i];
+    if (items) items[i] += h->prof_items[i];
     h->prof_ms[i] = 0;
     h->prof_n[i] = 0;
+    h->prof_items[i] = 0;
+  }
+  return FT_OK;
+}
+
+int ft_moe_debug_set(ft_moe *h, int what, int64_t value) {
+  if (int r = check_handle(h)) return r;
+  FT_CUDA(cudaDeviceSynchronize());
+  if (what == FT_DEBUG_HOLD_FILLS) {
+    const int v = value != 0;
+    FT_CUDA(cudaMemcpy(&h->ctr->hold_fills, &v, sizeof(v), cudaMemcpyHostToDevice));
+  } else if (what == FT_DEBUG_WAIT_NS) {
+    if (value < 1) return fail(FT_ERR_INVALID, "wait limit must be >= 1 ns");
+    const unsigned long long v = (unsigned long long)value;
+    FT_CUDA(cudaMemcpy(&h->ctr->wait_ns, &v, sizeof(v), cudaMemcpyHostToDevice));
+  } else {
+    return fail(FT_ERR_INVALID, "unknown debug setting %d", what);
   }
   return FT_OK;
 }

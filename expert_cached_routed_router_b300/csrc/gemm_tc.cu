@@ -64,6 +64,7 @@ struct TcArgs {
   int b_row_off;      // first B row of the matrix inside an entry (0 or 2*d)
   int up_off;         // gate/up: row offset of W_up from W_gate (d_ff)
   int shared_entry;   // entry index of the shared expert in its array (layer)
+  int by_item;        // 1: item u's weights are entry u of the B view (expanded MXFP4 scratch)
   int d, d_ff;
   uint16_t *h;        // gate/up output [rows][d_ff]
   const int32_t *tok; // down: token of each pair row
@@ -138,7 +139,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         decode_tile(a, n_work, t, u, nb, mt, mtiles);
         const WorkItem wi = a.work[u];
         const bool sh = wi.expert < 0;
-        const int entry = sh ? a.shared_entry : wi.slot;
+        const int entry = sh ? a.shared_entry : (a.by_item ? u : wi.slot);
         const void *mapB = sh ? (const void *)&tmBs : (const void *)&tmB;
         const int row_a = wi.q0 + mt * kTcM;
         const int row_b = entry * a.rows_per_entry + a.b_row_off + nb * (GATEUP ? 128 : BN);
@@ -327,8 +328,9 @@ static void tc_smem_attr(K kern, size_t smem) {
 
 void launch_tc_ffn(const TcMaps &maps, const WorkItem *work, DevCounters *ctr, int *prefix,
                    uint16_t *h, const int32_t *tok, const float *wq, float *acc, int d, int d_ff,
-                   int shared_entry, cudaStream_t s) {
+                   int shared_entry, bool by_item, cudaStream_t s) {
   TcArgs a{};
+  a.by_item = by_item ? 1 : 0;
   a.work = work;
   a.prefix = prefix;
   a.ctr = ctr;

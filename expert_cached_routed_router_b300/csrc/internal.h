@@ -34,23 +34,47 @@ void launch_route_decode(const uint16_t *x, const uint16_t *wr, const float *bia
 void launch_fill(const uint16_t *pool_dev, const CacheDesc *cache, const int32_t *fills,
                  DevCounters *ctr, size_t entry_bytes, int E, int max_fill, cudaStream_t s);
 
-// Decode expert FFN (T <= kGemvMaxTokens): gate/up GEMV + SwiGLU into h; down GEMV into the
-// fp32 per-row buffer y [(T*k + T)][d]; then the deterministic weighted combine into out.
-// fp4: the entries are MXFP4 (codes then block scales) instead of bf16
-void launch_gateup_gemv(const WorkItem *work, DevCounters *ctr, int max_work, const uint16_t *x,
-                        const int32_t *tok, uint16_t *h, int T, int d, int d_ff, bool fp4,
-                        cudaStream_t s);
-void launch_down_gemv(const WorkItem *work, DevCounters *ctr, int max_work, const uint16_t *h,
-                      float *y, int T, int d, int d_ff, bool fp4, cudaStream_t s);
-void launch_combine(const float *y, const float *w, const int32_t *inv, const DevCounters *ctr,
-                    uint16_t *out, int T, int k, int d, int shared, cudaStream_t s);
+// Decode expert path (T <= kGemvMaxTokens) in one persistent launch: miss fills from the
+// mapped pool, gate/up + SwiGLU into h, down into the fp32 per-row buffer y, and the
+// deterministic gate-weighted combine into out (decode.cu).
+struct DecodeArgs {
+  const WorkItem *work;     // [n_work]: hits, then misses (item n_hit + m uses fill m), shared
+  DevCounters *ctr;
+  const int32_t *fills;     // [n_fill][3] (destination entry, layer, expert)
+  const uint4 *pool;        // mapped host pool [L][E][entry]
+  const CacheDesc *cache;   // slot storage
+  const uint16_t *x;        // [T][d]
+  const int32_t *tok;       // [P + T] token of FFN row q
+  const float *w;           // [T][k] gates
+  const int32_t *inv;       // [P] FFN row of pair p
+  uint16_t *h;              // [P + T][d_ff]
+  float *y;                 // [P + T][d]
+  uint16_t *out;            // [T][d]
+  int32_t *sync;            // gu_done [kMaxE + 1] | fill_done [kMaxE] | dn_done [d]
+  int T, k, d, d_ff, E, shared;
+  int R_gu, R_dn;           // rows per gate/up and per down task (set by the launcher)
+  uint32_t stage_bytes, ring_bytes;
+  size_t entry_bytes;
+};
+constexpr int kSyncInts(int d) { return 2 * kMaxE + 1 + d; }
+
+struct DecodePlan {
+  bool xs;          // x staged in shared memory
+  uint32_t ring, stage;
+  int R_gu, R_dn, n_ib;
+  size_t smem;
+};
+DecodePlan plan_decode(int T, int d, int d_ff, bool fp4);
+int launch_decode_experts(DecodeArgs a, bool fp4, cudaStream_t s);
 
 // Grouped-GEMM expert FFN for larger T.
 void launch_gather_rows(const uint16_t *x, const int32_t *tok, uint16_t *xp, int rows, int d,
                         const DevCounters *ctr,
                         cudaStream_t s);
-void launch_cast_out(const float *acc, uint16_t *out, size_t n, const DevCounters *ctr,
-                     cudaStream_t s);
+// out = bf16(acc) (n % 8 == 0); with next != null also next = bf16(x + out), the residual
+// stream's input of the next prefill layer.
+void launch_cast_out(const float *acc, uint16_t *out, size_t n, const uint16_t *x, uint16_t *next,
+                     const DevCounters *ctr, cudaStream_t s);
 
 // Tensor maps of the tcgen05 grouped GEMMs for one weight buffer (slots, a prefill buffer):
 // A views of the gathered activations and of h, B views of the buffer's entries (rows of d
@@ -60,10 +84,15 @@ struct TcMaps {
 };
 // 2-D bf16 view [rows][inner] of base with a box of [box_rows][64] and 128-byte swizzle.
 bool make_tmap(CUtensorMap *m, const void *base, uint64_t inner, uint64_t rows, uint32_t box_rows);
-// gate/up then down (+ weighted red-add combine into acc) on the tensor cores.
+// gate/up then down (+ weighted red-add combine into acc) on the tensor cores.  by_item: the
+// weights of work item u are entry u of the maps' buffer (expanded MXFP4 scratch), otherwise
+// entry work[u].slot.
 void launch_tc_ffn(const TcMaps &maps, const WorkItem *work, DevCounters *ctr, int *prefix,
                    uint16_t *h, const int32_t *tok, const float *wq, float *acc, int d, int d_ff,
-                   int shared_entry, cudaStream_t s);
+                   int shared_entry, bool by_item, cudaStream_t s);
+// Expand the MXFP4 entries of the call's work items to bf16: item u -> scratch entry u.
+void launch_dequant_work(const WorkItem *work, const DevCounters *ctr, uint16_t *scratch, int d,
+                         int d_ff, int max_items, cudaStream_t s);
 
 // Record `code` and a message (with the CUDA error string if e != cudaSuccess) as this
 // thread's ft_last_error(); returns code.

@@ -9,9 +9,11 @@
 //
 // The scratch lives in the file-scope array below.  Every GPU that loads the library holds it
 // (1 MiB) until the process exits.  Host code cannot pass the array's name to a kernel: on the
-// host that name is only a stand-in, not a device address.  So the first call on each device,
-// with that device current, asks the runtime for the array's device address
-// (cudaGetSymbolAddress) and keeps it.  That first call should come before any stream capture.
+// host that name is only a stand-in, not a device address.  So a call asks the runtime for the
+// array's device address on the current device (cudaGetSymbolAddress) whenever its stream is
+// not capturing, and keeps it per device; a call on a capturing stream uses the kept address,
+// so the first call on each device must come before any stream capture.  Looking the address
+// up again on every uncaptured call keeps it right after cudaDeviceReset or a new context.
 //
 // All calls share the one array, which keeps the previous call's logits; a call overwrites all
 // T*E logits it reads, so nothing needs to start at zero.  Calls that overlap on the GPU (on
@@ -35,20 +37,30 @@ static __device__ __align__(256) float g_route_scratch[kMaxLogits];
 std::mutex g_mu;
 float *g_scratch_addr[kMaxDevices] = {};
 
-// Device address of g_route_scratch on the current device (looked up once per device).
-int scratch_address(float **out) {
+// Device address of g_route_scratch on the current device: looked up again when `s` is not
+// capturing (the runtime call may load the module, which a capture forbids), else the address
+// kept from the last uncaptured call on this device.
+int scratch_address(cudaStream_t s, float **out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return ftm::report_error(FT_ERR_CUDA, "cudaGetDevice", e);
   if (dev < 0 || dev >= kMaxDevices)
     return ftm::report_error(FT_ERR_INVALID, "device index out of range", cudaSuccess);
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  e = cudaStreamIsCapturing(s, &cs);
+  if (e != cudaSuccess) return ftm::report_error(FT_ERR_CUDA, "cudaStreamIsCapturing", e);
   std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_scratch_addr[dev]) {
+  if (cs == cudaStreamCaptureStatusNone) {
     void *p = nullptr;
     e = cudaGetSymbolAddress(&p, g_route_scratch);
     if (e != cudaSuccess)
       return ftm::report_error(FT_ERR_CUDA, "cudaGetSymbolAddress(routing scratch)", e);
     g_scratch_addr[dev] = static_cast<float *>(p);
+  } else if (!g_scratch_addr[dev]) {
+    return ftm::report_error(FT_ERR_STATE,
+                             "the first routing call on a device must come before any stream "
+                             "capture (it looks up the scratch address)",
+                             cudaSuccess);
   }
   *out = g_scratch_addr[dev];
   return FT_OK;
@@ -73,8 +85,8 @@ extern "C" int ft_route_topk_noalloc(const void *x, const void *Wr, const float 
   if ((((uintptr_t)x) | ((uintptr_t)Wr)) & 15)
     return ftm::report_error(FT_ERR_INVALID, "x and Wr must be 16-byte aligned", cudaSuccess);
   float *scratch = nullptr;
-  if (int r = scratch_address(&scratch)) return r;
   cudaStream_t s = (cudaStream_t)stream;
+  if (int r = scratch_address(s, &scratch)) return r;
   ftm::launch_router(static_cast<const uint16_t *>(x), static_cast<const uint16_t *>(Wr), bias,
                      scratch, T, E, d, s);
   ftm::launch_topk(scratch, idx, w, tie, T, E, k, s);

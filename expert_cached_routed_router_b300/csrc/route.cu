@@ -361,6 +361,8 @@ struct CtlSmem {
   int cand[kMaxE];  // eviction candidates below the threshold key
   int hist[2][256];
   unsigned long long wsum[32];
+  unsigned long long tick0;  // the LRU clock at the start of the call (read by thread 0)
+  int occupied0;             // occupied slots at the start of the call (read by thread 0)
   int misc[kMiscN];
   int pe[kPairSmem];    // expert of pair p (in-CTA top-k)
   float pv[kPairSmem];  // its logit
@@ -573,8 +575,20 @@ __device__ __forceinline__ void control_body(const ControlArgs &a, int mode,
   const bool lru = a.slot_table != nullptr;
   int *table = lru ? a.slot_table + (size_t)a.layer * E : nullptr;
   const int cur = (lru && tid < E) ? table[tid] : -1;  // issued early, used after grouping
-  if (tid == 0) a.ctr->call_status = 0;
+  if (tid == 0) {
+    a.ctr->call_status = 0;
+    // One read of the clock for the whole CTA, ordered before thread 0's update of it at the
+    // end of the call by the barriers below.  (Every thread reading ctr->tick itself raced with
+    // that update in calls without misses, which have no barrier in between.)
+    if (lru) {
+      sm.tick0 = a.ctr->tick;
+      sm.occupied0 = a.ctr->occupied;
+    }
+  }
   if (tid < kMiscN) sm.misc[tid] = 0;
+  // the decode expert kernel of the previous call has finished (this kernel waited for it):
+  // its completion counters start again from zero
+  for (int i = tid; i < a.n_sync; i += 1024) a.sync[i] = 0;
   for (int e = tid; e < E; e += 1024) sm.cnt[e] = 0;
   cta_sync();
 
@@ -630,7 +644,9 @@ __device__ __forceinline__ void control_body(const ControlArgs &a, int mode,
   const int n_hit = (int)((tot >> kFieldBits) & kFieldMask);
   const int n_miss = (int)(tot >> (2 * kFieldBits));
   const int n_touched = n_hit + n_miss;
-  const int trank = hrank + mrank;
+  // work list order: hits (ascending expert), then misses (ascending expert), then the
+  // shared expert; miss m is item n_hit + m and fill m
+  const int wrank = hit ? hrank : n_hit + mrank;
   if (mode == 1) {
     for (int e = tid; e <= E; e += 1024) sm.off[e] = a.offsets[e];
   } else {
@@ -717,7 +733,7 @@ __device__ __forceinline__ void control_body(const ControlArgs &a, int mode,
       }
       return;
     }
-    const unsigned long long tick0 = a.ctr->tick;
+    const unsigned long long tick0 = sm.tick0;
     if (a.freq) {
       if (touched) a.freq[(size_t)a.layer * E + tid] += 1u;
       if (tid == 0) {
@@ -744,7 +760,7 @@ __device__ __forceinline__ void control_body(const ControlArgs &a, int mode,
     if (n_miss > 0) {
       cta_sync();  // hit stamps written before eviction keys are read
       // the n_miss lowest free slots (none to look for once every slot is occupied)
-      if (a.ctr->occupied < cd.n_slots) {
+      if (sm.occupied0 < cd.n_slots) {
         for (int b0 = 0; b0 < cd.n_slots && n_free < n_miss; b0 += 1024) {
           const int s = b0 + tid;
           const bool f = s < cd.n_slots && cd.owner[s] < 0;
@@ -842,7 +858,7 @@ __device__ __forceinline__ void control_body(const ControlArgs &a, int mode,
     wi.count = cnt;
     wi.expert = tid;
     wi.slot = slot_of;
-    a.work[trank] = wi;
+    a.work[wrank] = wi;
   }
   cta_sync();
   if (tid == 0) {
@@ -857,6 +873,7 @@ __device__ __forceinline__ void control_body(const ControlArgs &a, int mode,
       a.work[nw++] = wi;
     }
     a.ctr->n_work = nw;
+    a.ctr->n_hit = n_hit;
     if (sm.misc[kMiscNear]) atomicAdd(&a.ctr->near_ties, (unsigned long long)sm.misc[kMiscNear]);
   }
 }

@@ -14,6 +14,8 @@ a combine - but print no formula; the plain reading, stated once here):
 4. Permutation grouped by expert: pairs p = t*k + j ordered by (expert, t, j) (``permutation``).
 5. Expert e: SwiGLU FFN  y = W_down^T (silu(W_gate^T x) * (W_up^T x)) in fp64 (``expert_ffn``).
 6. Combine: out[t] = sum_j w[t, j] * y_{idx[t, j]}(x_t)  (+ the shared expert with weight 1).
+7. Prefill residual stream (attention omitted): layer i+1 reads x_{i+1} = bf16(x_i + out_i)
+   (``residual_next``); the layers are checked one by one on the GPU's own x_i.
 """
 from __future__ import annotations
 
@@ -34,6 +36,21 @@ def bf16_to_f32(bits) -> np.ndarray:
     """bf16 bit patterns (uint16) -> exact float32 values."""
     u = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)
     return u.view(np.float32)
+
+
+def f32_to_bf16_bits(v) -> np.ndarray:
+    """float32 values -> bf16 bit patterns (uint16), rounded to nearest, ties to even
+    (finite values; the 16 dropped bits decide, with the kept last bit breaking ties)."""
+    u = np.asarray(v, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    u = u + np.uint64(0x7FFF) + ((u >> np.uint64(16)) & np.uint64(1))
+    return (u >> np.uint64(16)).astype(np.uint16)
+
+
+def residual_next(x_bits, out_bits) -> np.ndarray:
+    """Input of the next layer of a prefill's residual stream (attention omitted): the layer's
+    bf16 input plus its bf16 output, added in fp32 and rounded to bf16 (nearest even)."""
+    s = bf16_to_f32(x_bits) + bf16_to_f32(out_bits)      # one IEEE fp32 add
+    return f32_to_bf16_bits(s)
 
 
 def router_logits(x_bits, wr_bits, bias=None) -> np.ndarray:

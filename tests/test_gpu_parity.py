@@ -254,17 +254,50 @@ def test_admission_across_resizes(fp4):
     st.close()
 
 
-def test_mxfp4_refuses_grouped_gemm_and_prefill():
+@pytest.mark.parametrize("T", [17, 40, 300, 700])
+def test_mxfp4_grouped_gemm(T):
+    """MXFP4 entries in calls with more tokens than the decode path takes: the touched entries
+    (after their fills) are expanded to bf16 and run through the tcgen05 grouped GEMMs.
+    Routing, fills and cache state bit-exact; every output row within tolerance of the oracle's
+    expert network on the dequantized weights (T = 700 gives 3+ M-tiles per group)."""
+    cfg = Config(L=2, E=8, k=2, d=256, d_ff=384, n_slots=10, seed=15, fp4=True)
+    st = make_stack(cfg, max_tokens=1024)
+    sim = olru.SlotCacheSim(cfg.L, cfg.E, cfg.n_slots, cfg.entry_bytes, prewarm=True)
+    for l in (1, 0, 1):
+        x = ft_synth.activations(15, 10 * T + l, T, cfg.d)
+        out = _run(st, l, x)
+        ref = oracle_layer(cfg, l, x)
+        assert_routing_equal(st, ref, T)
+        code, hits, fills = sim.access(l, ref["idx"].ravel())
+        assert code == olru.OK
+        np.testing.assert_array_equal(st.fills(), np.array([f[:3] for f in fills],
+                                                            dtype=np.int32).reshape(-1, 3))
+        assert_cache_equal(st, sim)
+        assert_out_close(out_bits_to_f64(out), ref["out"])
+    assert sim.misses > 0 and st.status() == 0
+    st.close()
+
+
+def test_mxfp4_prefill():
+    """MXFP4 prefill: the double buffer carries the 4-bit entries over the host link (17/32 of
+    the bf16 bytes), each layer is expanded to bf16 for the grouped GEMMs; residual stream and
+    teacher-forced oracle as for bf16 entries."""
     import torch
-    from expert_cached_routed_router_b300 import FtError
-    cfg = Config(L=1, E=16, k=2, d=256, d_ff=128, n_slots=16, seed=15, fp4=True)
-    st = make_stack(cfg, max_tokens=64)
-    x = to_dev_bf16(ft_synth.activations(15, 0, 17, cfg.d))
-    out = torch.empty_like(x)
-    with pytest.raises(FtError):
-        st.forward(0, x, out)
-    with pytest.raises(FtError):
-        st.prefill(0, 1, x, torch.empty((1, 17, cfg.d), dtype=torch.int16, device="cuda"))
+    cfg = Config(L=3, E=8, k=2, d=256, d_ff=256, n_slots=4, seed=19, fp4=True)
+    T = 300
+    st = make_stack(cfg, max_tokens=T)
+    x = ft_synth.activations(19, 0, T, cfg.d)
+    out = torch.empty((cfg.L, T, cfg.d), dtype=torch.int16, device="cuda")
+    st.prefill(0, cfg.L, to_dev_bf16(x), out)
+    torch.cuda.synchronize()
+    xin = x
+    for l in range(cfg.L):
+        ref = oracle_layer(cfg, l, xin)
+        assert_out_close(out_bits_to_f64(out[l]), ref["out"])
+        xin = omoe.residual_next(xin, out[l].cpu().numpy().view(np.uint16))
+    assert_routing_equal(st, ref, T)
+    assert st.prefill_bytes() == (cfg.L * cfg.E * cfg.entry_bytes, 0)
+    assert st.status() == 0
     st.close()
 
 
@@ -330,7 +363,11 @@ def test_shared_expert():
 
 
 def test_prefill_double_buffer_matches_oracle():
-    """Prefill reads the double buffer only: every layer on the same x, the cache untouched."""
+    """Prefill reads the double buffer only, and chains the layers through the residual
+    stream: layer l+1 reads x_{l+1} = bf16(x_l + out_l).  Every layer matches the oracle on the
+    GPU's own input (teacher forcing, the input rebuilt from the outputs by the oracle's
+    residual step); the last layer's logits are bit-exact, so the GPU's chained input is too;
+    the cache is untouched."""
     import torch
     cfg = Config(L=3, E=16, k=2, d=256, d_ff=128, n_slots=4, seed=7)
     T = 600
@@ -342,16 +379,42 @@ def test_prefill_double_buffer_matches_oracle():
     st.prefill(0, 3, xd, out)
     torch.cuda.synchronize()
     rows = np.arange(0, T, 5)
+    xin = x
     for l in range(3):
-        ref = oracle_layer(cfg, l, x, tokens=rows)
+        ref = oracle_layer(cfg, l, xin, tokens=rows)
         assert_out_close(out_bits_to_f64(out[l])[rows], ref["out"])
-    assert_routing_equal(st, oracle_layer(cfg, 2, x, tokens=[]), T)  # last layer's routing
+        if l == 2:
+            np.testing.assert_array_equal(st.logits(T).view(np.uint32),
+                                          ref["logits"].view(np.uint32))
+            assert_routing_equal(st, ref, T)  # last layer's routing
+        xin = omoe.residual_next(xin, out[l].cpu().numpy().view(np.uint16))
     after = st.cache_state()
     for a, b in zip(before[:3], after[:3]):
         np.testing.assert_array_equal(a, b)
     c, k, w = st.prefill_timing()
     assert c > 0 and k > 0 and w > 0
     assert st.prefill_bytes() == (3 * cfg.E * cfg.entry_bytes, 0)
+    st.close()
+
+
+@pytest.mark.parametrize("T", [1, 16])
+def test_prefill_short_prompts(T):
+    """Prompts as short as decode batches still take the grouped-GEMM path in prefill (one
+    M-tile, mostly empty rows) and chain through the residual stream."""
+    import torch
+    cfg = Config(L=2, E=16, k=2, d=256, d_ff=128, n_slots=4, seed=8)
+    st = make_stack(cfg, max_tokens=64)
+    x = ft_synth.activations(8, T, T, cfg.d)
+    out = torch.empty((2, T, cfg.d), dtype=torch.int16, device="cuda")
+    st.prefill(0, 2, to_dev_bf16(x), out)
+    torch.cuda.synchronize()
+    xin = x
+    for l in range(2):
+        ref = oracle_layer(cfg, l, xin)
+        assert_out_close(out_bits_to_f64(out[l]), ref["out"])
+        xin = omoe.residual_next(xin, out[l].cpu().numpy().view(np.uint16))
+    assert_routing_equal(st, ref, T)
+    assert st.status() == 0
     st.close()
 
 
@@ -380,9 +443,11 @@ def test_prefill_topup_from_cache_slots():
     st.prefill(0, cfg.L, to_dev_bf16(x), out)
     torch.cuda.synchronize()
     rows = np.arange(1, T, 7)
+    xin = x
     for l in range(cfg.L):
-        ref = oracle_layer(cfg, l, x, tokens=rows)
+        ref = oracle_layer(cfg, l, xin, tokens=rows)
         assert_out_close(out_bits_to_f64(out[l])[rows], ref["out"])
+        xin = omoe.residual_next(xin, out[l].cpu().numpy().view(np.uint16))
     after = st.cache_state()
     for a, b in zip(before, after):
         np.testing.assert_array_equal(a, b)
@@ -543,3 +608,40 @@ def test_decode_step_graph_capture_matches_eager():
     for a, b in zip(st_e, st_g):
         np.testing.assert_array_equal(np.asarray(a), np.asarray(b))
     assert s_e["misses"] == s_g["misses"] > 0 and s_e["hits"] == s_g["hits"]
+
+
+def test_decode_wait_times_out_and_context_recovers():
+    """Every cross-CTA wait of the decode expert kernel is bounded.  With a host-set flag the
+    kernel copies its fills but never reports them done, so the work waiting for them runs out
+    of its (shortened) wait limit: the call records FT_ERR_TIMEOUT and returns, the GPU context
+    stays usable, and the next calls (flag cleared) match the oracle and its simulator."""
+    import time
+    import torch
+    import expert_cached_routed_router_b300 as ftm
+    cfg = Config(L=2, E=16, k=2, d=256, d_ff=128, n_slots=8, seed=12)
+    st = make_stack(cfg, max_tokens=16)   # prewarm: layer 0's experts 0..7 in slots 0..7
+    sim = olru.SlotCacheSim(cfg.L, cfg.E, cfg.n_slots, cfg.entry_bytes, prewarm=True)
+    st.debug_set(ftm.FT_DEBUG_WAIT_NS, 20_000_000)
+    st.debug_set(ftm.FT_DEBUG_HOLD_FILLS, 1)
+    x = ft_synth.activations(12, 0, 3, cfg.d)
+    t0 = time.perf_counter()
+    _run(st, 1, x)                         # layer 1: every touched expert misses
+    elapsed = time.perf_counter() - t0
+    assert st.status() == ftm.FT_ERR_TIMEOUT
+    assert elapsed < 10.0
+    ref = oracle_layer(cfg, 1, x)
+    assert sim.access(1, ref["idx"].ravel())[0] == olru.OK
+    assert_cache_equal(st, sim)            # the control ran; only the expert work timed out
+    st.debug_set(ftm.FT_DEBUG_HOLD_FILLS, 0)
+    st.debug_set(ftm.FT_DEBUG_WAIT_NS, 4_000_000_000)
+    st.stats_reset()
+    for l, t in ((1, 3), (0, 5), (1, 4)):  # hits on the (copied) entries, then new misses
+        xv = ft_synth.activations(12, 10 + t, t, cfg.d)
+        out = _run(st, l, xv)
+        ref = oracle_layer(cfg, l, xv)
+        assert sim.access(l, ref["idx"].ravel())[0] == olru.OK
+        assert_routing_equal(st, ref, t)
+        assert_out_close(out_bits_to_f64(out), ref["out"])
+        assert_cache_equal(st, sim)
+    assert st.status() == 0
+    st.close()

@@ -1,4 +1,4 @@
-"""The seeded input generator: published splitmix64 vectors, Box-Muller moments, bf16 rounding."""
+"""The seeded input generator: published splitmix64 vectors, Irwin-Hall normal moments, bf16 rounding."""
 import numpy as np
 
 import ft_synth
