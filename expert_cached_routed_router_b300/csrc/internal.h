@@ -50,21 +50,26 @@ struct DecodeArgs {
   uint16_t *h;              // [P + T][d_ff]
   float *y;                 // [P + T][d]
   uint16_t *out;            // [T][d]
-  int32_t *sync;            // gu_done [kMaxE + 1] | fill_done [kMaxE] | dn_done [d]
+  int32_t *sync;            // phase counters and flags [kSyncPhaseInts] | fill_done [kMaxE]
   int T, k, d, d_ff, E, shared;
+  int max_items;            // largest possible n_work: min(E, T*k) + shared (set by the launcher)
+  int n_rows;               // FFN rows: T*k, plus T for the shared expert (set by the launcher)
   int R_gu, R_dn;           // rows per gate/up and per down task (set by the launcher)
-  uint32_t stage_bytes, ring_bytes;
+  uint32_t stage_bytes;
+  int n_stages;
   size_t entry_bytes;
 };
-constexpr int kSyncInts(int d) { return 2 * kMaxE + 1 + d; }
+constexpr int kSyncPhaseInts = 192;  // three counters and three flags, one 128-byte line each
+constexpr int kSyncInts(int d) { return (void)d, kSyncPhaseInts + kMaxE; }
 
 struct DecodePlan {
   bool xs;          // x staged in shared memory
   uint32_t ring, stage;
+  int n_stages;
   int R_gu, R_dn, n_ib;
   size_t smem;
 };
-DecodePlan plan_decode(int T, int d, int d_ff, bool fp4);
+DecodePlan plan_decode(int T, int d, int d_ff, int max_items, int n_rows, bool fp4);
 int launch_decode_experts(DecodeArgs a, bool fp4, cudaStream_t s);
 
 // Grouped-GEMM expert FFN for larger T.

@@ -11,6 +11,7 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <algorithm>
 #include <type_traits>
 
 #include "internal.h"
@@ -344,7 +345,6 @@ void launch_perm_multi(const ControlArgs &a, int32_t *chunk_scratch, cudaStream_
 // follow such a loop is preceded by __syncwarp() (cta_sync), so warps reach it converged.
 // ---------------------------------------------------------------------------------------
 constexpr int kStampSmem = 2048;                     // slots whose keys fit in shared memory
-constexpr int kTopkSmem = 4096;                      // T*E logits for the in-CTA top-k
 constexpr int kPairSmem = kGemvMaxTokens * kMaxK;    // pairs of the in-CTA top-k
 constexpr int kFieldBits = 21;                       // packed per-expert scan fields
 constexpr unsigned long long kFieldMask = (1ull << kFieldBits) - 1;
@@ -366,9 +366,8 @@ struct CtlSmem {
   int misc[kMiscN];
   int pe[kPairSmem];    // expert of pair p (in-CTA top-k)
   float pv[kPairSmem];  // its logit
-  float next[kGemvMaxTokens];  // (k+1)-th logit of token t
+  float pw[kPairSmem];  // its gate
   union {
-    float logit[kTopkSmem];
     unsigned long long key[kStampSmem];
     struct {              // admission decisions, by miss rank m / victim rank j
       unsigned mf[kMaxE];   // count of miss m
@@ -413,58 +412,89 @@ __device__ __forceinline__ unsigned long long cta_scan_u64(unsigned long long v,
   return v;
 }
 
-// Top-k of T tokens inside the CTA (T*E <= kTopkSmem, T <= kGemvMaxTokens): every (t, e)
-// counts the experts that beat it under (logit descending, id ascending); rank r < k puts
-// e at position r.  Gates w_j = exp(l_j - l_0) / sum_i exp(l_i - l_0); near-tie when two
-// adjacent selected logits, or the k-th and (k+1)-th, differ by <= kNearTie (in double).
-// Leaves pair p = t*k + j in sm.pe / sm.pv and returns thread p's gate.
-__device__ __forceinline__ float topk_cta(const ControlArgs &a, const float *logits,
-                                          CtlSmem &sm) {
-  const int T = a.T, E = a.E, k = a.k, n = T * E, tid = threadIdx.x;
-  for (int i = tid; i < n; i += 1024) sm.u.logit[i] = __ldcg(logits + i);
-  // a position no expert ranks into (NaN logits compare false) stays -1: an invalid pair
+// Top-k of T <= kGemvMaxTokens tokens inside the CTA, one warp per token: k+1 rounds of a
+// warp argmax under (logit descending, expert id ascending) over the token's logits (NV per
+// lane), the (k+1)-th only for the near-tie report.  Gates w_j = exp(l_j - l_0) / sum_i
+// exp(l_i - l_0); near-tie when two adjacent selected logits, or the k-th and (k+1)-th,
+// differ by <= kNearTie (in double).  Leaves pair p = t*k + j in sm.pe / sm.pv / sm.pw (an
+// expert no round selects - all remaining logits NaN - stays -1: an invalid pair) and writes
+// idx, w and tie.  O(T k E) work, against O(T E^2) for ranking every (t, e) by counting.
+template <int NV>
+__device__ __forceinline__ void topk_warps(const ControlArgs &a, const float *logits, CtlSmem &sm) {
+  const int T = a.T, E = a.E, k = a.k, tid = threadIdx.x;
+  const int lane = tid & 31, t = tid >> 5;
   for (int p = tid; p < T * k; p += 1024) {
     sm.pe[p] = -1;
     sm.pv[p] = 0.f;
-  }
-  if (tid < kGemvMaxTokens) sm.next[tid] = 0.f;
-  cta_sync();
-  for (int i = tid; i < n; i += 1024) {
-    const int t = i / E, e = i - t * E;
-    const float v = sm.u.logit[i];
-    const float *row = sm.u.logit + t * E;
-    int rank = 0;
-    for (int e2 = 0; e2 < E && rank <= k; ++e2) {
-      const float v2 = row[e2];
-      rank += (v2 > v || (v2 == v && e2 < e)) ? 1 : 0;
-    }
-    if (rank < k) {
-      sm.pe[t * k + rank] = e;
-      sm.pv[t * k + rank] = v;
-    } else if (rank == k) {
-      sm.next[t] = v;
-    }
+    sm.pw[p] = 0.f;
   }
   cta_sync();
-  float w = 0.f;
-  if (tid < T * k) {
-    const int t = tid / k, j = tid - t * k;
-    const float *pv = sm.pv + t * k;
-    const float l0 = pv[0];
-    float sum = 0.f;
-    for (int i = 0; i < k; ++i) sum += expf(pv[i] - l0);
-    w = expf(pv[j] - l0) / sum;
-    const_cast<int32_t *>(a.idx)[tid] = sm.pe[tid];
-    const_cast<float *>(a.w)[tid] = w;
-    if (j == 0) {
-      bool near = false;
-      for (int i = 0; i + 1 < k; ++i) near = near || ((double)pv[i] - (double)pv[i + 1]) <= kNearTie;
-      if (k < E) near = near || ((double)pv[k - 1] - (double)sm.next[t]) <= kNearTie;
-      const_cast<uint8_t *>(a.tie)[t] = near ? 1 : 0;
-      if (near) atomicAdd(&sm.misc[kMiscNear], 1);
+  if (t < T) {
+    const float *row = logits + (size_t)t * E;
+    float v[NV];
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+      const int e = lane + 32 * i;
+      v[i] = (e < E) ? __ldcg(row + e) : -INFINITY;
+    }
+    uint32_t taken = 0;  // bit i: expert lane+32i already selected
+    float sel_v = 0.f;   // lane j keeps the j-th selected logit
+    int sel_i = -1;
+    float next_v = -INFINITY;
+    const int rounds = (k < E) ? k + 1 : k;
+    for (int r = 0; r < rounds; ++r) {
+      float bv = -INFINITY;
+      int bi = 0x7fffffff;
+#pragma unroll
+      for (int i = 0; i < NV; ++i) {
+        const int e = lane + 32 * i;
+        if (e < E && !((taken >> i) & 1u) && better(v[i], e, bv, bi)) {
+          bv = v[i];
+          bi = e;
+        }
+      }
+#pragma unroll
+      for (int off = 16; off >= 1; off >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+        if (better(ov, oi, bv, bi)) {
+          bv = ov;
+          bi = oi;
+        }
+      }
+      if (r < k) {
+        if (bi < E && (bi & 31) == lane) taken |= 1u << (bi >> 5);
+        if (lane == r) {
+          sel_v = bv;
+          sel_i = bi < E ? bi : -1;
+        }
+      } else {
+        next_v = bv;
+      }
+    }
+    const float l0 = __shfl_sync(0xffffffffu, sel_v, 0);
+    const float ex = (lane < k) ? expf(sel_v - l0) : 0.f;
+    float sum = ex;
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+    const float nxt_sel = __shfl_down_sync(0xffffffffu, sel_v, 1);
+    bool near = false;
+    if (lane + 1 < k) near = ((double)sel_v - (double)nxt_sel) <= kNearTie;
+    if (lane == k - 1 && k < E) near = near || ((double)sel_v - (double)next_v) <= kNearTie;
+    const bool any_near = __any_sync(0xffffffffu, near);
+    if (lane < k) {
+      const float w = ex / sum;
+      sm.pe[t * k + lane] = sel_i;
+      sm.pv[t * k + lane] = sel_v;
+      sm.pw[t * k + lane] = w;
+      const_cast<int32_t *>(a.idx)[t * k + lane] = sel_i;
+      const_cast<float *>(a.w)[t * k + lane] = w;
+    }
+    if (lane == 0) {
+      const_cast<uint8_t *>(a.tie)[t] = any_near ? 1 : 0;
+      if (any_near) atomicAdd(&sm.misc[kMiscNear], 1);
     }
   }
-  return w;
 }
 
 // The nv smallest eviction keys (stamp of an occupied slot with stamp <= tick0; others are
@@ -567,6 +597,7 @@ __device__ bool select_victims(const CacheDesc &cd, unsigned long long tick0, in
 
 // mode: 0 = pairs from idx in global memory (P <= kPermSingleMax), 1 = perm_ready (counts
 // and offsets from a multi-CTA pass), 2 = in-CTA top-k from `logits` (fused decode).
+template <int NV>
 __device__ __forceinline__ void control_body(const ControlArgs &a, int mode,
                                              const float *logits) {
   __shared__ CtlSmem sm;
@@ -595,7 +626,9 @@ __device__ __forceinline__ void control_body(const ControlArgs &a, int mode,
   // 1. counts (and, below, offsets and grouping)
   float my_w = 0.f;
   if (mode == 2) {
-    my_w = topk_cta(a, logits, sm);
+    topk_warps<NV>(a, logits, sm);
+    cta_sync();
+    my_w = tid < P ? sm.pw[tid] : 0.f;
     if (tid < P) {
       const int e = sm.pe[tid];
       if (e >= 0 && e < E)
@@ -879,83 +912,44 @@ __device__ __forceinline__ void control_body(const ControlArgs &a, int mode,
 }
 
 __global__ void __launch_bounds__(1024) k_control(ControlArgs a, int perm_ready) {
-  control_body(a, perm_ready ? 1 : 0, nullptr);
+  control_body<1>(a, perm_ready ? 1 : 0, nullptr);
 }
 
 // ---------------------------------------------------------------------------------------
-// Decode routing in one launch (T <= kGemvMaxTokens): every CTA computes a block of router
-// logits; the CTA that finishes last (atomic arrival counter, no waiting) runs the top-k of
-// all T tokens and then the control body above.  With T*E <= kTopkSmem the top-k runs on
-// the whole CTA from shared memory; otherwise one warp per token.
+// Decode routing in one launch (T <= kGemvMaxTokens).  The T*E router logits are one warp
+// task each, spread over up to one CTA per SM (task = CTA + warp * grid, so a call with few
+// logits uses one warp on each of many SMs: their loads run in parallel); the CTA that
+// finishes last (atomic arrival counter, no waiting) runs the top-k of every token, one warp
+// per token, and then the control body above.
 // ---------------------------------------------------------------------------------------
-template <int TT, int EE, int NV>
+template <int NV>
 __global__ void __launch_bounds__(1024) k_route_decode(const uint16_t *__restrict__ x,
                                                        const uint16_t *__restrict__ wr,
                                                        const float *__restrict__ bias,
                                                        float *__restrict__ logits,
                                                        ControlArgs a) {
   pdl_trigger();
-  const int T = a.T, E = a.E;
-  const int lane = threadIdx.x & 31;
-  const int n_eb = (E + EE - 1) / EE;
-  const int n_tasks = ((T + TT - 1) / TT) * n_eb;
-  const int task = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+  const int T = a.T, E = a.E, d = a.d, nchunk = d >> 3;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int n_tasks = T * E, G = gridDim.x;
   // The router weights change only through ft_moe_load_router (a copy, fully ordered):
   // stage this warp's rows in L2 while the previous kernel finishes.  x may be that
   // kernel's output and the bias a copy queued after it, so both are read after the wait.
-  if (task < n_tasks) {
-    const int e0 = (task % n_eb) * EE, nchunk = a.d >> 3;
-    for (int c = lane; c < nchunk; c += 32)
-#pragma unroll
-      for (int j = 0; j < EE; ++j)
-        if (e0 + j < E) prefetch_l2(wr + (size_t)(e0 + j) * a.d + (size_t)c * 8);
+  for (int task = blockIdx.x + warp * G; task < n_tasks; task += 32 * G) {
+    const int e = task % E;
+    for (int c = lane; c < nchunk; c += 32) prefetch_l2(wr + (size_t)e * d + (size_t)c * 8);
   }
   pdl_wait();
-  if (task < n_tasks) {
-    const int tb = task / n_eb, eb = task - tb * n_eb;
-    const int t0 = tb * TT, e0 = eb * EE;
-    float bv[EE];
+  for (int task = blockIdx.x + warp * G; task < n_tasks; task += 32 * G) {
+    const int t = task / E, e = task - t * E;
+    const uint4 *xr = reinterpret_cast<const uint4 *>(x + (size_t)t * d);
+    const uint4 *wrr = reinterpret_cast<const uint4 *>(wr + (size_t)e * d);
+    float acc = 0.f;  // lane lam: chunks lam, lam+32, ... in order, features in order
+#pragma unroll 8
+    for (int c = lane; c < nchunk; c += 32) acc = dot8_seq(__ldg(xr + c), __ldg(wrr + c), acc);
 #pragma unroll
-    for (int j = 0; j < EE; ++j) bv[j] = (bias && e0 + j < E) ? __ldg(bias + e0 + j) : 0.f;
-    float acc[TT][EE];
-#pragma unroll
-    for (int i = 0; i < TT; ++i)
-#pragma unroll
-      for (int j = 0; j < EE; ++j) acc[i][j] = 0.f;
-    const int d = a.d, nchunk = d >> 3;
-#pragma unroll(TT * EE <= 2 ? 4 : 2)
-    for (int c = lane; c < nchunk; c += 32) {
-      uint4 xv[TT], wv[EE];
-#pragma unroll
-      for (int i = 0; i < TT; ++i)
-        xv[i] = (t0 + i < T) ? __ldg(reinterpret_cast<const uint4 *>(x + (size_t)(t0 + i) * d) + c)
-                             : make_uint4(0, 0, 0, 0);
-#pragma unroll
-      for (int j = 0; j < EE; ++j)
-        wv[j] = (e0 + j < E) ? __ldg(reinterpret_cast<const uint4 *>(wr + (size_t)(e0 + j) * d) + c)
-                             : make_uint4(0, 0, 0, 0);
-#pragma unroll
-      for (int i = 0; i < TT; ++i)
-#pragma unroll
-        for (int j = 0; j < EE; ++j) acc[i][j] = dot8_seq(xv[i], wv[j], acc[i][j]);
-    }
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1)
-#pragma unroll
-      for (int i = 0; i < TT; ++i)
-#pragma unroll
-        for (int j = 0; j < EE; ++j)
-          acc[i][j] = acc[i][j] + __shfl_xor_sync(0xffffffffu, acc[i][j], off);
-#pragma unroll
-    for (int i = 0; i < TT; ++i)
-#pragma unroll
-      for (int j = 0; j < EE; ++j) {
-        if (lane == ((i * EE + j) & 31) && t0 + i < T && e0 + j < E) {
-          float v = acc[i][j];
-          if (bias) v = v + bv[j];
-          logits[(size_t)(t0 + i) * E + e0 + j] = v;
-        }
-      }
+    for (int off = 16; off >= 1; off >>= 1) acc = acc + __shfl_xor_sync(0xffffffffu, acc, off);
+    if (lane == 0) logits[task] = bias ? acc + __ldg(bias + e) : acc;
   }
   // the last CTA to arrive continues
   __shared__ int s_last;
@@ -969,32 +963,26 @@ __global__ void __launch_bounds__(1024) k_route_decode(const uint16_t *__restric
   if (!s_last) return;
   __threadfence();
   if (threadIdx.x == 0) a.ctr->route_arrive = 0;
-  if (T * E <= kTopkSmem) {
-    control_body(a, 2, logits);
-  } else {
-    const int warp = threadIdx.x >> 5;
-    for (int t = warp; t < T; t += 32)
-      topk_warp<NV>(logits + (size_t)t * E, E, a.k, const_cast<int32_t *>(a.idx) + (size_t)t * a.k,
-                    const_cast<float *>(a.w) + (size_t)t * a.k, const_cast<uint8_t *>(a.tie) + t);
-    cta_sync();
-    control_body(a, 0, nullptr);
+  control_body<NV>(a, 2, logits);
+}
+
+static int route_sm_count() {
+  static int n = 0;
+  if (!n) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 148;
   }
+  return n;
 }
 
 void launch_route_decode(const uint16_t *x, const uint16_t *wr, const float *bias, float *logits,
                          const ControlArgs &a, cudaStream_t s) {
+  const int grid = std::max(1, std::min(a.T * a.E, route_sm_count()));
   dispatch_nv(a.E, [&](auto nv) {
     constexpr int NV = decltype(nv)::value;
-    auto go = [&](auto kern, int tt, int ee) {
-      const int tasks = ((a.T + tt - 1) / tt) * ((a.E + ee - 1) / ee);
-      launch_pdl(kern, dim3((tasks + 31) / 32), dim3(1024), 0, s, x, wr, bias, logits, a);
-    };
-    if (a.T == 1)
-      go(k_route_decode<1, 1, NV>, 1, 1);
-    else if (a.T <= 2)
-      go(k_route_decode<2, 2, NV>, 2, 2);
-    else
-      go(k_route_decode<4, 2, NV>, 4, 2);
+    launch_pdl(k_route_decode<NV>, dim3(grid), dim3(1024), 0, s, x, wr, bias, logits, a);
   });
 }
 
