@@ -199,7 +199,26 @@ struct TaskList {
 // Consumer bodies, bf16 entries.
 // ---------------------------------------------------------------------------------------
 
-// G token rows against one gate row and one up row held in shared memory.
+// The 8 bf16 values of a 16-byte chunk as fp32, in feature order.
+__device__ __forceinline__ void unpack8(uint4 v, float (&f)[8]) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+
+// acc + sum_i a[i] * b[i], sequentially in feature order (the order dot8_seq uses).
+__device__ __forceinline__ float fma8(const float (&a)[8], const float (&b)[8], float acc) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc = fmaf(a[i], b[i], acc);
+  return acc;
+}
+
+// G token rows against one gate row and one up row held in shared memory.  Each chunk of the
+// two weight rows is unpacked once, each token's chunk of x once, and shared by the gate and
+// up sums (per-sum order: chunks lane, lane+32, ..., features in order, as dot8_seq).
 template <int G, bool XS>
 __device__ __forceinline__ void gateup_dots(const uint4 *__restrict__ g, const uint4 *__restrict__ uu,
                                             const uint4 *__restrict__ xs, const int32_t *tk,
@@ -212,13 +231,16 @@ __device__ __forceinline__ void gateup_dots(const uint4 *__restrict__ g, const u
     row[t] = (t < n) ? tk[t] * nchunk : 0;
   }
   for (int ch = lane; ch < nchunk; ch += 32) {
-    const uint4 gv = g[ch], uv = uu[ch];
+    float gf[8], uf[8];
+    unpack8(g[ch], gf);
+    unpack8(uu[ch], uf);
 #pragma unroll
     for (int t = 0; t < G; ++t) {
       if (t < n) {
-        const uint4 xv = XS ? xs[row[t] + ch] : __ldg(xs + row[t] + ch);
-        ag[t] = dot8_seq(gv, xv, ag[t]);
-        au[t] = dot8_seq(uv, xv, au[t]);
+        float xf[8];
+        unpack8(XS ? xs[row[t] + ch] : __ldg(xs + row[t] + ch), xf);
+        ag[t] = fma8(xf, gf, ag[t]);
+        au[t] = fma8(xf, uf, au[t]);
       }
     }
   }
@@ -248,16 +270,17 @@ __device__ __forceinline__ void down_dots(const uint8_t *__restrict__ st, int ro
 #pragma unroll
     for (int t = 0; t < G; ++t) part[r][t] = 0.f;
   for (int ch = lane; ch < nchunk; ch += 32) {
-    uint4 hv[G];
+    float hf[G][8];  // each token's chunk of h, unpacked once for all rows
 #pragma unroll
     for (int t = 0; t < G; ++t)
-      hv[t] = (t < n) ? ld_cg16(hq + (size_t)t * d_ff + 8 * ch) : make_uint4(0, 0, 0, 0);
+      unpack8((t < n) ? ld_cg16(hq + (size_t)t * d_ff + 8 * ch) : make_uint4(0, 0, 0, 0), hf[t]);
 #pragma unroll
     for (int r = 0; r < kDownRows; ++r) {
       if (r < rows) {
-        const uint4 wv = reinterpret_cast<const uint4 *>(st + (size_t)r * d_ff * 2)[ch];
+        float wf[8];
+        unpack8(reinterpret_cast<const uint4 *>(st + (size_t)r * d_ff * 2)[ch], wf);
 #pragma unroll
-        for (int t = 0; t < G; ++t) part[r][t] = dot8_seq(wv, hv[t], part[r][t]);
+        for (int t = 0; t < G; ++t) part[r][t] = fma8(wf, hf[t], part[r][t]);
       }
     }
   }
@@ -293,11 +316,16 @@ __device__ __forceinline__ void down_dots1(const uint8_t *__restrict__ st, int r
   for (int i = 0; i < kHPre; ++i) {
     const int ch = lane + 32 * i;
     if (ch < nchunk) {
+      float hf[8];
+      unpack8(hp[i], hf);
 #pragma unroll
-      for (int r = 0; r < kDownRows; ++r)
-        if (r < rows)
-          part[r][0] = dot8_seq(reinterpret_cast<const uint4 *>(st + (size_t)r * d_ff * 2)[ch],
-                                hp[i], part[r][0]);
+      for (int r = 0; r < kDownRows; ++r) {
+        if (r < rows) {
+          float wf[8];
+          unpack8(reinterpret_cast<const uint4 *>(st + (size_t)r * d_ff * 2)[ch], wf);
+          part[r][0] = fma8(wf, hf, part[r][0]);
+        }
+      }
     }
   }
   for (int ch = lane + 32 * kHPre; ch < nchunk; ch += 32) {
@@ -325,17 +353,6 @@ __device__ __forceinline__ void down_dots1(const uint8_t *__restrict__ st, int r
 __device__ __forceinline__ void decode8(uint32_t w, float (&v)[8]) {
 #pragma unroll
   for (int e = 0; e < 8; ++e) v[e] = e2m1_f32(w >> (4 * e));
-}
-
-// acc + sum_e v[e] * x[e] over 8 bf16 inputs x (one uint4), in input order.
-__device__ __forceinline__ float dot8_vals(const float (&v)[8], uint4 xv, float acc) {
-  const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    acc = fmaf(v[2 * i], __uint_as_float(xw[i] << 16), acc);
-    acc = fmaf(v[2 * i + 1], __uint_as_float(xw[i] & 0xFFFF0000u), acc);
-  }
-  return acc;
 }
 
 template <int G, bool XS>
@@ -367,9 +384,10 @@ __device__ __forceinline__ void gateup_dots_fp4(const uint4 *__restrict__ g,
       for (int t = 0; t < G; ++t) {
         if (t < n) {
           const int xi = row[t] + 4 * ch + q;
-          const uint4 xv = XS ? xs[xi] : __ldg(xs + xi);
-          bg[t] = dot8_vals(vg, xv, bg[t]);
-          bu[t] = dot8_vals(vu, xv, bu[t]);
+          float xf[8];  // unpacked once for the gate and the up sum
+          unpack8(XS ? xs[xi] : __ldg(xs + xi), xf);
+          bg[t] = fma8(vg, xf, bg[t]);
+          bu[t] = fma8(vu, xf, bu[t]);
         }
       }
     }
@@ -391,7 +409,8 @@ __device__ __forceinline__ void gateup_dots_fp4(const uint4 *__restrict__ g,
 }
 
 // rows W_down rows: their codes at `codes` (d_ff/2 bytes per row), their scales at `scales`
-// (d_ff/32 bytes per row).
+// (d_ff/32 bytes per row).  Per 32-input block: each token's h words are unpacked once for
+// all rows; each row's block sum runs over its 32 inputs in order, then takes the block scale.
 template <int G>
 __device__ __forceinline__ void down_dots_fp4(const uint8_t *__restrict__ codes,
                                               const uint8_t *__restrict__ scales, int rows,
@@ -404,31 +423,39 @@ __device__ __forceinline__ void down_dots_fp4(const uint8_t *__restrict__ codes,
 #pragma unroll
     for (int t = 0; t < G; ++t) part[r][t] = 0.f;
   for (int ch = lane; ch < nblk; ch += 32) {
-    uint4 hv[G][4];
+    uint4 qr[kDownRows];
 #pragma unroll
-    for (int t = 0; t < G; ++t)
+    for (int r = 0; r < kDownRows; ++r)
+      qr[r] = r < rows ? reinterpret_cast<const uint4 *>(codes + r * cb)[ch] : make_uint4(0, 0, 0, 0);
+    float b[kDownRows][G];
 #pragma unroll
-      for (int q = 0; q < 4; ++q)
-        hv[t][q] = (t < n) ? ld_cg16(hq + (size_t)t * d_ff + 32 * ch + 8 * q)
-                           : make_uint4(0, 0, 0, 0);
+    for (int r = 0; r < kDownRows; ++r)
+#pragma unroll
+      for (int t = 0; t < G; ++t) b[r][t] = 0.f;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      float hf[G][8];
+#pragma unroll
+      for (int t = 0; t < G; ++t)
+        unpack8((t < n) ? ld_cg16(hq + (size_t)t * d_ff + 32 * ch + 8 * q) : make_uint4(0, 0, 0, 0),
+                hf[t]);
+#pragma unroll
+      for (int r = 0; r < kDownRows; ++r) {
+        if (r < rows) {
+          const uint32_t w = q == 0 ? qr[r].x : (q == 1 ? qr[r].y : (q == 2 ? qr[r].z : qr[r].w));
+          float v[8];
+          decode8(w, v);
+#pragma unroll
+          for (int t = 0; t < G; ++t) b[r][t] = fma8(v, hf[t], b[r][t]);
+        }
+      }
+    }
 #pragma unroll
     for (int r = 0; r < kDownRows; ++r) {
       if (r < rows) {
-        const uint4 qr = reinterpret_cast<const uint4 *>(codes + r * cb)[ch];
-        const uint32_t w[4] = {qr.x, qr.y, qr.z, qr.w};
-        float b[G];
-#pragma unroll
-        for (int t = 0; t < G; ++t) b[t] = 0.f;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          float v[8];
-          decode8(w[q], v);
-#pragma unroll
-          for (int t = 0; t < G; ++t) b[t] = dot8_vals(v, hv[t][q], b[t]);
-        }
         const float sc = e8m0_f32(scales[r * sbr + ch]);
 #pragma unroll
-        for (int t = 0; t < G; ++t) part[r][t] = fmaf(b[t], sc, part[r][t]);
+        for (int t = 0; t < G; ++t) part[r][t] = fmaf(b[r][t], sc, part[r][t]);
       }
     }
   }
