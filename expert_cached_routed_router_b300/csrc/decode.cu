@@ -637,7 +637,10 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode_experts(const DecodeA
       for (int i = (it > r.n ? it - r.n : 0); i < it; ++i) {
         int s, use;
         r.slot_of(i, s, use);
-        mbar_wait(&r.full[s], (uint32_t)(use & 1));
+        // suspended between polls: a spinning thread takes shared-memory cycles from the
+        // consumers still at work
+        for (long j = 0; j < (1L << 22); ++j)
+          if (mbar_try_wait_sleep(&r.full[s], (uint32_t)(use & 1), 1000)) break;
       }
     }
     return;

@@ -345,6 +345,8 @@ void launch_perm_multi(const ControlArgs &a, int32_t *chunk_scratch, cudaStream_
 // follow such a loop is preceded by __syncwarp() (cta_sync), so warps reach it converged.
 // ---------------------------------------------------------------------------------------
 constexpr int kStampSmem = 2048;                     // slots whose keys fit in shared memory
+constexpr int kSlotBits = 21;                        // slot id bits of a packed victim key
+constexpr int kFewVictims = 4;                       // victims found by repeated minima
 constexpr int kPairSmem = kGemvMaxTokens * kMaxK;    // pairs of the in-CTA top-k
 constexpr int kFieldBits = 21;                       // packed per-expert scan fields
 constexpr unsigned long long kFieldMask = (1ull << kFieldBits) - 1;
@@ -412,6 +414,38 @@ __device__ __forceinline__ unsigned long long cta_scan_u64(unsigned long long v,
   return v;
 }
 
+// Warp of token t, lane j < k holding the j-th selected expert sel_i and logit sel_v (lanes
+// >= k: anything), next_v the (k+1)-th logit (-inf if none): gates w_j = exp(l_j - l_0) /
+// sum_i exp(l_i - l_0), near-tie when two adjacent selected logits, or the k-th and
+// (k+1)-th, differ by <= kNearTie (in double); pairs t*k + j into sm.pe / pv / pw and idx,
+// w, tie.
+__device__ __forceinline__ void gates_and_ties(const ControlArgs &a, CtlSmem &sm, int t, int lane,
+                                               int sel_i, float sel_v, float next_v) {
+  const int k = a.k, E = a.E;
+  const float l0 = __shfl_sync(0xffffffffu, sel_v, 0);
+  const float ex = (lane < k) ? expf(sel_v - l0) : 0.f;
+  float sum = ex;
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+  const float nxt_sel = __shfl_down_sync(0xffffffffu, sel_v, 1);
+  bool near = false;
+  if (lane + 1 < k) near = ((double)sel_v - (double)nxt_sel) <= kNearTie;
+  if (lane == k - 1 && k < E) near = near || ((double)sel_v - (double)next_v) <= kNearTie;
+  const bool any_near = __any_sync(0xffffffffu, near);
+  if (lane < k) {
+    const float w = ex / sum;
+    sm.pe[t * k + lane] = sel_i;
+    sm.pv[t * k + lane] = sel_v;
+    sm.pw[t * k + lane] = w;
+    const_cast<int32_t *>(a.idx)[t * k + lane] = sel_i;
+    const_cast<float *>(a.w)[t * k + lane] = w;
+  }
+  if (lane == 0) {
+    const_cast<uint8_t *>(a.tie)[t] = any_near ? 1 : 0;
+    if (any_near) atomicAdd(&sm.misc[kMiscNear], 1);
+  }
+}
+
 // Top-k of T <= kGemvMaxTokens tokens inside the CTA, one warp per token: k+1 rounds of a
 // warp argmax under (logit descending, expert id ascending) over the token's logits (NV per
 // lane), the (k+1)-th only for the near-tie report.  Gates w_j = exp(l_j - l_0) / sum_i
@@ -472,36 +506,65 @@ __device__ __forceinline__ void topk_warps(const ControlArgs &a, const float *lo
         next_v = bv;
       }
     }
-    const float l0 = __shfl_sync(0xffffffffu, sel_v, 0);
-    const float ex = (lane < k) ? expf(sel_v - l0) : 0.f;
-    float sum = ex;
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-    const float nxt_sel = __shfl_down_sync(0xffffffffu, sel_v, 1);
-    bool near = false;
-    if (lane + 1 < k) near = ((double)sel_v - (double)nxt_sel) <= kNearTie;
-    if (lane == k - 1 && k < E) near = near || ((double)sel_v - (double)next_v) <= kNearTie;
-    const bool any_near = __any_sync(0xffffffffu, near);
-    if (lane < k) {
-      const float w = ex / sum;
-      sm.pe[t * k + lane] = sel_i;
-      sm.pv[t * k + lane] = sel_v;
-      sm.pw[t * k + lane] = w;
-      const_cast<int32_t *>(a.idx)[t * k + lane] = sel_i;
-      const_cast<float *>(a.w)[t * k + lane] = w;
+    gates_and_ties(a, sm, t, lane, sel_i, sel_v, next_v);
+  }
+}
+
+
+// The same top-k by ranking, for small T*E^2: each (t, e) counts the logits of token t that
+// come before it under (logit descending, expert id ascending); rank j < k puts e at pair
+// t*k + j and rank k is the (k+1)-th logit of the near-tie report.  A NaN logit is never
+// ranked, and never counts as coming before another (in the argmax rounds a NaN never wins),
+// so every selection matches the rounds'.  O(T E^2) work over the whole CTA: cheaper than
+// k+1 dependent warp reductions when T*E^2 <= kRankWork.
+constexpr int kRankWork = 1 << 16;
+constexpr int kRankSmem = kStampSmem * 2;  // floats of the logits staged in sm.u.key
+__device__ __forceinline__ void topk_rank(const ControlArgs &a, const float *logits, CtlSmem &sm) {
+  const int T = a.T, E = a.E, k = a.k, tid = threadIdx.x, lane = tid & 31;
+  float *lg = reinterpret_cast<float *>(sm.u.key);
+  float *nxt = reinterpret_cast<float *>(&sm.hist[0][0]);
+  for (int i = tid; i < T * E; i += 1024) lg[i] = __ldcg(logits + i);
+  for (int p = tid; p < T * k; p += 1024) {
+    sm.pe[p] = -1;
+    sm.pv[p] = -INFINITY;
+    sm.pw[p] = 0.f;
+  }
+  if (tid < T) nxt[tid] = -INFINITY;
+  cta_sync();
+  for (int i = tid; i < T * E; i += 1024) {
+    const int t = i / E, e = i - t * E;
+    const float v = lg[i];
+    if (!(v == v)) continue;
+    const float *row = lg + t * E;
+    int r = 0;
+#pragma unroll 8
+    for (int j = 0; j < E; ++j) {
+      const float u = row[j];
+      r += (u > v || (u == v && j < e)) ? 1 : 0;
     }
-    if (lane == 0) {
-      const_cast<uint8_t *>(a.tie)[t] = any_near ? 1 : 0;
-      if (any_near) atomicAdd(&sm.misc[kMiscNear], 1);
+    if (r < k) {
+      sm.pe[t * k + r] = e;
+      sm.pv[t * k + r] = v;
+    } else if (r == k) {
+      nxt[t] = v;
     }
+  }
+  cta_sync();
+  const int t = tid >> 5;
+  if (t < T) {
+    const int sel_i = lane < k ? sm.pe[t * k + lane] : -1;
+    const float sel_v = lane < k ? sm.pv[t * k + lane] : 0.f;
+    gates_and_ties(a, sm, t, lane, sel_i, sel_v, nxt[t]);
   }
 }
 
 // The nv smallest eviction keys (stamp of an occupied slot with stamp <= tick0; others are
-// not eligible) in increasing (stamp, slot) order -> out[0 .. nv).  A radix select (8-bit
-// digits from the top bit of tick0) finds the nv-th smallest stamp v*; the slots with a
-// smaller stamp are ranked among themselves, the ones at v* follow in slot order.
-// Returns false (and writes nothing) if fewer than nv slots are eligible.
+// not eligible) in increasing (stamp, slot) order -> out[0 .. nv).  Up to kFewVictims of
+// them (keys in shared memory, stamps below 2^43): nv rounds of a CTA minimum of the packed
+// (stamp, slot) key, each taking its slot out.  Otherwise a radix select (8-bit digits from
+// the top bit of tick0) finds the nv-th smallest stamp v*; the slots with a smaller stamp
+// are ranked among themselves, the ones at v* follow in slot order.  Returns false if fewer
+// than nv slots are eligible (out is then left in an unspecified state).
 __device__ bool select_victims(const CacheDesc &cd, unsigned long long tick0, int nv, int *out,
                                CtlSmem &sm) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -520,6 +583,37 @@ __device__ bool select_victims(const CacheDesc &cd, unsigned long long tick0, in
     sm.misc[kMiscCand] = 0;
   }
   cta_sync();
+  if (in_smem && nv <= kFewVictims && tick0 < (1ull << (64 - kSlotBits))) {
+    for (int j = 0; j < nv; ++j) {
+      unsigned long long best = ~0ull;
+      for (int s = tid; s < n; s += 1024) {
+        const unsigned long long kk = sm.u.key[s];
+        if (kk != ~0ull) best = min(best, (kk << kSlotBits) | (unsigned long long)s);
+      }
+#pragma unroll
+      for (int off = 16; off >= 1; off >>= 1) best = min(best, __shfl_xor_sync(0xffffffffu, best, off));
+      if (lane == 0) sm.wsum[warp] = best;
+      cta_sync();
+      if (warp == 0) {
+        best = sm.wsum[lane];
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1)
+          best = min(best, __shfl_xor_sync(0xffffffffu, best, off));
+        if (lane == 0) {
+          if (best == ~0ull) {
+            sm.misc[kMiscErr] = 1;
+          } else {
+            const int s = (int)(best & ((1ull << kSlotBits) - 1));
+            out[j] = s;
+            sm.u.key[s] = ~0ull;
+          }
+        }
+      }
+      cta_sync();
+      if (sm.misc[kMiscErr]) return false;
+    }
+    return true;
+  }
   const int nbits = 64 - __clzll(tick0 | 1ull);
   unsigned long long prefix = 0;  // digits of v* fixed so far
   int need = nv;                  // rank of v* among the keys that match the prefix
@@ -626,7 +720,10 @@ __device__ __forceinline__ void control_body(const ControlArgs &a, int mode,
   // 1. counts (and, below, offsets and grouping)
   float my_w = 0.f;
   if (mode == 2) {
-    topk_warps<NV>(a, logits, sm);
+    if (a.T * a.E * a.E <= kRankWork && a.T * a.E <= kRankSmem)
+      topk_rank(a, logits, sm);
+    else
+      topk_warps<NV>(a, logits, sm);
     cta_sync();
     my_w = tid < P ? sm.pw[tid] : 0.f;
     if (tid < P) {

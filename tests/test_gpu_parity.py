@@ -82,6 +82,29 @@ def test_decode_edge_shapes(E, k, T, n_slots):
     st.close()
 
 
+@pytest.mark.parametrize("T,d_ff,shared", [(16, 2048, 1), (4, 512, 1), (1, 2048, 0)])
+def test_decode_misses_with_shared_expert_every_row(T, d_ff, shared):
+    """Decode calls with misses (and a shared expert) at 16, 4 and 1 tokens with d_ff = 2048
+    and 512: routing, fills and cache state bit-exact, every output row within tolerance."""
+    cfg = Config(L=2, E=24, k=4, d=256, d_ff=d_ff, n_slots=24, n_shared=shared, seed=14)
+    st = make_stack(cfg, max_tokens=16, pool=gpu_host_pool(cfg))
+    sim = olru.SlotCacheSim(cfg.L, cfg.E, cfg.n_slots, cfg.entry_bytes, prewarm=True)
+    for step in range(4):
+        for l in (0, 1):
+            x = ft_synth.activations(14, 100 * T + 10 * step + l, T, cfg.d)
+            out = _run(st, l, x)
+            ref = oracle_layer(cfg, l, x)
+            assert_routing_equal(st, ref, T)
+            code, hits, fills = sim.access(l, ref["idx"].ravel())
+            assert code == olru.OK
+            np.testing.assert_array_equal(st.fills(), np.array([f[:3] for f in fills],
+                                                                dtype=np.int32).reshape(-1, 3))
+            assert_cache_equal(st, sim)
+            assert_out_close(out_bits_to_f64(out), ref["out"])
+    assert sim.misses > 0 and st.status() == 0
+    st.close()
+
+
 def test_victims_beyond_shared_memory_staging():
     """More than 2,048 slots: the control reads the eviction keys from global memory."""
     cfg = Config(L=40, E=64, k=4, d=128, d_ff=128, n_slots=2100, seed=13)
@@ -486,6 +509,40 @@ def test_chained_layers_read_previous_output(T):
         assert_routing_equal(st, ref, T)   # the last call's routing
         assert_cache_equal(st, sim)
     assert st.stats()["status"] == 0 and sim.misses > 0
+    st.close()
+
+
+@pytest.mark.parametrize("E,k,T", [(32, 4, 1), (32, 4, 3), (128, 8, 4), (128, 8, 16),
+                                   (512, 8, 1), (64, 6, 40)])
+@pytest.mark.parametrize("pattern", ["ties_inside", "ties_across_k"])
+def test_topk_exact_ties_minus_inf_and_nan_logits(E, k, T, pattern):
+    """Router biases that force exact logit ties (1e30 absorbs the dot product), -inf logits
+    and a NaN logit: the order (logit descending, expert id ascending), the (k+1)-th logit of
+    the near-tie flag and NaN never being selected match the oracle for the ranking top-k
+    (small T*E^2), the warp-argmax top-k (T = 16 at E = 128, E = 512) and the grouped path
+    (T = 40)."""
+    import torch
+    cfg = Config(L=1, E=E, k=k, d=128, d_ff=128, n_slots=min(E, 256), seed=19)
+    st = make_stack(cfg, max_tokens=64)
+    bias = np.zeros(E, np.float32)
+    top = [5, 9, 17, 30]                                 # 4 tied experts, all selected
+    if pattern == "ties_across_k":
+        top = [10 + 3 * i for i in range(k + 2)]         # k + 2 tied: the tie spans rank k
+    bias[top] = 1e30
+    bias[[1, 2, E - 1]] = -np.inf
+    bias[7] = np.nan
+    st.set_router_bias(0, torch.from_numpy(bias).cuda())
+    x = ft_synth.activations(19, T, T, cfg.d)
+    out = _run(st, 0, x)
+    ref = oracle_layer(cfg, 0, x, bias=bias, tokens=np.arange(min(T, 3)))
+    lg, rl = st.logits(T), ref["logits"]
+    fin = ~np.isnan(rl)                                  # a NaN's payload is not compared
+    np.testing.assert_array_equal(np.isnan(lg), ~fin)
+    np.testing.assert_array_equal(lg[fin].view(np.uint32), rl[fin].view(np.uint32))
+    assert_routing_equal(st, ref, T)
+    assert not np.isin(7, ref["idx"]) and ref["tie"].all()
+    assert_out_close(out_bits_to_f64(out)[ref["tokens"]], ref["out"])
+    assert st.status() == 0
     st.close()
 
 
