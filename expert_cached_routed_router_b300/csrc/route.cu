@@ -369,7 +369,7 @@ struct CtlSmem {
   int pe[kPairSmem];    // expert of pair p (in-CTA top-k)
   float pv[kPairSmem];  // its logit
   float pw[kPairSmem];  // its gate
-  union {
+  union alignas(16) {
     unsigned long long key[kStampSmem];
     struct {              // admission decisions, by miss rank m / victim rank j
       unsigned mf[kMaxE];   // count of miss m
@@ -519,8 +519,11 @@ __device__ __forceinline__ void topk_warps(const ControlArgs &a, const float *lo
 // k+1 dependent warp reductions when T*E^2 <= kRankWork.
 constexpr int kRankWork = 1 << 16;
 constexpr int kRankSmem = kStampSmem * 2;  // floats of the logits staged in sm.u.key
-__device__ __forceinline__ void topk_rank(const ControlArgs &a, const float *logits, CtlSmem &sm) {
-  const int T = a.T, E = a.E, k = a.k, tid = threadIdx.x, lane = tid & 31;
+// Stage the logits and clear the pairs; the caller's next block barrier orders this before
+// topk_rank (so the loads overlap the rest of the control prologue).
+__device__ __forceinline__ void topk_rank_stage(const ControlArgs &a, const float *logits,
+                                                CtlSmem &sm) {
+  const int T = a.T, E = a.E, k = a.k, tid = threadIdx.x;
   float *lg = reinterpret_cast<float *>(sm.u.key);
   float *nxt = reinterpret_cast<float *>(&sm.hist[0][0]);
   for (int i = tid; i < T * E; i += 1024) lg[i] = __ldcg(logits + i);
@@ -530,24 +533,49 @@ __device__ __forceinline__ void topk_rank(const ControlArgs &a, const float *log
     sm.pw[p] = 0.f;
   }
   if (tid < T) nxt[tid] = -INFINITY;
-  cta_sync();
-  for (int i = tid; i < T * E; i += 1024) {
-    const int t = i / E, e = i - t * E;
-    const float v = lg[i];
-    if (!(v == v)) continue;
-    const float *row = lg + t * E;
-    int r = 0;
-#pragma unroll 8
-    for (int j = 0; j < E; ++j) {
-      const float u = row[j];
-      r += (u > v || (u == v && j < e)) ? 1 : 0;
-    }
+}
+__device__ __forceinline__ bool use_topk_rank(const ControlArgs &a) {
+  return a.T * a.E * a.E <= kRankWork && a.T * a.E <= kRankSmem;
+}
+__device__ __forceinline__ void topk_rank(const ControlArgs &a, CtlSmem &sm) {
+  const int T = a.T, E = a.E, k = a.k, tid = threadIdx.x, lane = tid & 31;
+  const float *lg = reinterpret_cast<const float *>(sm.u.key);
+  float *nxt = reinterpret_cast<float *>(&sm.hist[0][0]);
+  auto place = [&](int t, int e, float v, int r) {
     if (r < k) {
       sm.pe[t * k + r] = e;
       sm.pv[t * k + r] = v;
     } else if (r == k) {
       nxt[t] = v;
     }
+  };
+  const int pairs = T * E;
+  for (int i = tid; i < pairs; i += 1024) {
+    const int t = i / E, e = i - t * E;
+    const float v = lg[i];
+    if (!(v == v)) continue;
+    const float *row = lg + t * E;
+    int r = 0;
+    if ((E & 3) == 0) {
+      // four independent counts over 16-byte rows (row t starts at a multiple of 16 bytes)
+      int r1 = 0, r2 = 0, r3 = 0;
+#pragma unroll 4
+      for (int j = 0; j < E; j += 4) {
+        const float4 u = *reinterpret_cast<const float4 *>(row + j);
+        r += (u.x > v || (u.x == v && j < e)) ? 1 : 0;
+        r1 += (u.y > v || (u.y == v && j + 1 < e)) ? 1 : 0;
+        r2 += (u.z > v || (u.z == v && j + 2 < e)) ? 1 : 0;
+        r3 += (u.w > v || (u.w == v && j + 3 < e)) ? 1 : 0;
+      }
+      r += r1 + r2 + r3;
+    } else {
+#pragma unroll 8
+      for (int j = 0; j < E; ++j) {
+        const float u = row[j];
+        r += (u > v || (u == v && j < e)) ? 1 : 0;
+      }
+    }
+    place(t, e, v, r);
   }
   cta_sync();
   const int t = tid >> 5;
@@ -715,13 +743,15 @@ __device__ __forceinline__ void control_body(const ControlArgs &a, int mode,
   // its completion counters start again from zero
   for (int i = tid; i < a.n_sync; i += 1024) a.sync[i] = 0;
   for (int e = tid; e < E; e += 1024) sm.cnt[e] = 0;
+  const bool rank_topk = mode == 2 && use_topk_rank(a);
+  if (rank_topk) topk_rank_stage(a, logits, sm);
   cta_sync();
 
   // 1. counts (and, below, offsets and grouping)
   float my_w = 0.f;
   if (mode == 2) {
-    if (a.T * a.E * a.E <= kRankWork && a.T * a.E <= kRankSmem)
-      topk_rank(a, logits, sm);
+    if (rank_topk)
+      topk_rank(a, sm);
     else
       topk_warps<NV>(a, logits, sm);
     cta_sync();
