@@ -55,9 +55,10 @@ def test_exhaustive_single_key_traces(cap):
 
 
 def test_random_multi_expert_traces():
-    """Calls touching several experts (hits-then-misses order matters), with prewarm."""
+    """10,000 random traces of calls touching several experts (hits-then-misses order matters),
+    with and without prewarm, against the brute-force LRU model."""
     rng = np.random.default_rng(0)
-    for _ in range(1500):
+    for _ in range(10_000):
         L, E = int(rng.integers(1, 4)), int(rng.integers(2, 6))
         cap = int(rng.integers(1, L * E + 2))
         trace = []
