@@ -20,7 +20,11 @@
 // shared expert), down of the resident items, gate/up of the missed items, down of the missed
 // items.  Task g goes to CTA g mod gridDim.x, and a CTA takes its tasks in increasing g.  The
 // waits, all bounded (globaltimer, abort flag):
-//   - a missed item's tasks wait (producer) until its whole entry is filled: fill_done[m];
+//   - a missed item's gate/up tasks wait (producer) until the gate/up rows of its entry are
+//     filled (fill_done[m]), its down tasks until the rest is too (fill_dn[m]); the fill warps
+//     copy the gate/up rows of every missed entry before any down rows, so the missed experts'
+//     gate/up runs while their down rows still cross the host link (bf16 entries; an MXFP4
+//     entry, whose scales follow all its codes, is one region);
 //   - the down tasks of resident items wait (consumer) until every consumer warp of the grid
 //     has finished its gate/up tasks of resident items (phase counter A), those of missed
 //     items until every warp has finished its gate/up tasks of missed items (counter C);
@@ -522,7 +526,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode_experts(const DecodeA
   // finished their gate/up tasks of resident items (A), of missed items (C), and all their
   // tasks (Y); a flag per phase set by the last CTA to count itself
   int *g_cnt = a.sync, *g_flag = a.sync + 3 * 32;
-  int *fill_done = a.sync + kSyncPhaseInts;
+  int *fill_done = a.sync + kSyncPhaseInts, *fill_dn = fill_done + kMaxE;
   TaskList tl;
   tl.n_hit = n_hit;
   tl.n_miss = n_fill;
@@ -534,6 +538,11 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode_experts(const DecodeA
   tl.nC = tl.n_miss * tl.n_jb;
   tl.n = tl.nA + tl.nB + tl.nC + tl.n_miss * tl.n_ib;
   const int fill_chunks = (int)((a.entry_bytes / 16 + kFillChunk - 1) / kFillChunk);
+  // chunks holding W_gate and W_up (the first 4*d*d_ff bytes of a bf16 entry), then the rest
+  const int gu_chunks =
+      FP4 ? fill_chunks
+          : min(fill_chunks, (int)(((size_t)4 * d * d_ff / 16 + kFillChunk - 1) / kFillChunk));
+  const int dn_chunks = fill_chunks - gu_chunks;
 
   if (warp > kProducerWarp) {
     // ------------------------------------------------------------ fill warps
@@ -543,9 +552,17 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode_experts(const DecodeA
     const size_t ev = a.entry_bytes / 16;
     const CacheDesc *cd = a.cache;
     uint4 *slots = reinterpret_cast<uint4 *>(cd->slots);
+    const int gu_total = n_fill * gu_chunks;
     for (int c = fw; c < n_fill * fill_chunks; c += n_fw) {
-      const int m = c / fill_chunks;
-      const int cc = c - m * fill_chunks;
+      int m, cc;
+      if (c < gu_total) {
+        m = c / gu_chunks;
+        cc = c - m * gu_chunks;
+      } else {
+        const int c2 = c - gu_total;
+        m = c2 / dn_chunks;
+        cc = gu_chunks + (c2 - m * dn_chunks);
+      }
       const int dst_e = a.fills[3 * m], l = a.fills[3 * m + 1], e = a.fills[3 * m + 2];
       const uint4 *src = a.pool + ((size_t)l * a.E + e) * ev;
       uint4 *dst = slots + (size_t)dst_e * ev;
@@ -562,7 +579,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode_experts(const DecodeA
       fence_proxy_async_global();
       __threadfence();
       __syncwarp();
-      if (lane == 0 && !hold) atomicAdd(&fill_done[m], 1);
+      if (lane == 0 && !hold) atomicAdd(cc < gu_chunks ? &fill_done[m] : &fill_dn[m], 1);
     }
     return;
   }
@@ -572,7 +589,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode_experts(const DecodeA
     if (lane == 0) {
       bool ok = true;
       int it = 0;
-      int ready_m = -1;
+      int ready_gu = -1, ready_dn = -1;
       for (int g = blockIdx.x; g < tl.n; g += gridDim.x, ++it) {
         const Task t = tl.at(g);
         int s, use;
@@ -581,13 +598,21 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode_experts(const DecodeA
           ok = false;
           break;
         }
-        if (t.miss >= 0 && t.miss != ready_m) {
-          if (!wait_count(&fill_done[t.miss], fill_chunks, limit, abort)) {
+        if (t.miss >= 0 && t.miss != ready_gu) {
+          if (!wait_count(&fill_done[t.miss], gu_chunks, limit, abort)) {
             ok = false;
             break;
           }
           fence_proxy_async_global();
-          ready_m = t.miss;
+          ready_gu = t.miss;
+        }
+        if (t.miss >= 0 && t.down && dn_chunks > 0 && t.miss != ready_dn) {
+          if (!wait_count(&fill_dn[t.miss], dn_chunks, limit, abort)) {
+            ok = false;
+            break;
+          }
+          fence_proxy_async_global();
+          ready_dn = t.miss;
         }
         const uint8_t *W = reinterpret_cast<const uint8_t *>(items[t.u].W);
         uint8_t *st = r.stage(s);

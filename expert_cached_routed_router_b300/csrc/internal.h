@@ -50,7 +50,8 @@ struct DecodeArgs {
   uint16_t *h;              // [P + T][d_ff]
   float *y;                 // [P + T][d]
   uint16_t *out;            // [T][d]
-  int32_t *sync;            // phase counters and flags [kSyncPhaseInts] | fill_done [kMaxE]
+  int32_t *sync;            // phase counters and flags [kSyncPhaseInts] | fill_done [kMaxE] |
+                            // fill_dn [kMaxE]
   int T, k, d, d_ff, E, shared;
   int max_items;            // largest possible n_work: min(E, T*k) + shared (set by the launcher)
   int n_rows;               // FFN rows: T*k, plus T for the shared expert (set by the launcher)
@@ -60,7 +61,7 @@ struct DecodeArgs {
   size_t entry_bytes;
 };
 constexpr int kSyncPhaseInts = 192;  // three counters and three flags, one 128-byte line each
-constexpr int kSyncInts(int d) { return (void)d, kSyncPhaseInts + kMaxE; }
+constexpr int kSyncInts(int d) { return (void)d, kSyncPhaseInts + 2 * kMaxE; }
 
 struct DecodePlan {
   bool xs;          // x staged in shared memory
